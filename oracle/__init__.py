@@ -1,0 +1,18 @@
+"""CPU oracle for the Qwen3-0.6B-shape causal decoder hot path.
+
+TEST INFRASTRUCTURE ONLY.  The tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` are the only code that may import
+or run anything in this package.  The CUDA library and its Python binding never
+import, link or call it, and this package imports nothing from them: callers
+hand it plain arrays (the seeded inputs) and compare its results with the GPU's.
+
+Every function computes in float64 (see ``decoder.py`` for the reading of the
+pages this follows).  Parity is pinned by ``tests/test_oracle_pins.py``.
+"""
+from .decoder import (DecoderOracle, rms_norm, rope_inv_freq, rope_neox, causal_gqa_attention,
+                      swiglu, inputs_embeds, tied_lm_head, greedy_argmax, fake_token_len)
+from .metrics import step_metrics, parity_gate
+
+__all__ = ["DecoderOracle", "rms_norm", "rope_inv_freq", "rope_neox", "causal_gqa_attention",
+           "swiglu", "inputs_embeds", "tied_lm_head", "greedy_argmax", "fake_token_len",
+           "step_metrics", "parity_gate"]
