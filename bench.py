@@ -1,0 +1,334 @@
+"""Benchmark of the Qwen3-0.6B-shape decoder hot path on one GB300 (or N replicas).
+
+One step = one pass of the whole path over one synthetic request of the
+workload: prefill of the prompt (embedding gather + audio splice, 28 layers,
+tied lm_head + argmax on the last position), then the workload's greedy decode
+steps at batch 1 (KV-cache decode, lm_head + argmax; the argmax is fed back on
+the device).  Default workload: the Fun-ASR-Nano-like short clip, a 64-position
+prompt (20 ids, 23 audio rows, 21 ids) and 64 decode steps.
+
+value  = decode tokens/s (B = 1) over the timed steps, device-timed with CUDA
+         events on the decoder's stream, inputs resident in HBM.
+e2e    = the same metric through the C ABI with host buffers: pinned host ids
+         and audio rows copied in every step, every decode step's argmax read
+         back to the host and fed back as the next token, and the last
+         logits vector copied out.
+The weights (1.19 GB) are larger than L2 (129 MB), so no L2 flush is needed
+between steps.
+
+--impl reference times the CPU oracle (float64 numpy) on the host cores on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tok/s & ms/token (B=1, Qwen3-0.6B shape), prefill tok/s, % HBM roofline"
+UNIT = "tok/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="funasr_nano_short")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def workload_desc(wl):
+    return {"workload": wl.name, "description": wl.description, "prompt_positions": wl.n_prompt,
+            "audio_rows": wl.n_audio, "audio_offset": wl.audio_offset, "decode_steps": wl.n_decode,
+            "batch": wl.batch, "l2": "inputs larger than L2 (1.19 GB of bf16 weights per step), no flush"}
+
+
+def decode_step_bytes(shape, L):
+    """Algorithmic HBM bytes of one batch-1 decode step whose KV length after the
+    append is L: every weight once (embedding row only for the gather; the full
+    embedding for the tied head), the KV cache read [0, L-1), the new K/V slot
+    written, logits written."""
+    H, D, F = shape.hidden, shape.head_dim, shape.ffn
+    per_layer = (shape.qkv_rows * H + H * shape.n_q_heads * D + 2 * F * H + H * F + 2 * H + 2 * D) * 2
+    weights = shape.n_layers * per_layer + shape.vocab * H * 2 + H * 2 + H * 2
+    kv = (L - 1) * shape.kv_bytes_per_position + shape.kv_bytes_per_position
+    return weights + kv + shape.vocab * 4
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) >= 9 and f[1].replace(".", "").isdigit():
+                    rows.append(f)
+        except Exception:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except Exception:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": sorted(reasons),
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())
+                if any(r[3].replace(".", "").isdigit() for r in rows) else None}
+
+
+def oracle_sample(wl, n_decode, seed=0, reps=1):
+    """Times the CPU oracle (as it stands) on prefill + n_decode greedy steps of wl."""
+    import numpy as np
+    import torch
+    from concurrent.futures import ThreadPoolExecutor
+    import oracle
+    from qwen3_prefill_kv_gb300 import synth
+    w = synth.make_weights(wl.shape, seed)
+
+    def f64(t):
+        return t.to(torch.float64).numpy()
+    with ThreadPoolExecutor(os.cpu_count() or 1) as ex:
+        layers = [dict(zip(l.keys(), ex.map(f64, l.values()))) for l in w.layers]
+        emb = f64(w.embed)
+    orc = oracle.DecoderOracle(wl.shape, {"embed": emb, "final_norm": f64(w.final_norm), "layers": layers})
+    p = synth.make_prompt(wl, seed)
+    audio = p.audio.to(torch.float64).numpy()
+    res = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        z = orc.prefill(p.ids.numpy(), audio, p.audio_offset)
+        t1 = time.perf_counter()
+        for _ in range(n_decode):
+            z = orc.decode_step(oracle.greedy_argmax(z))
+        t2 = time.perf_counter()
+        res.append((t1 - t0, t2 - t1))
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return res, cores
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from qwen3_prefill_kv_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    n_dec = 8
+    res, cores = oracle_sample(wl, n_dec, reps=args.warmup + args.steps)
+    timed = res[args.warmup:]
+    dec_s = sum(d for _, d in timed)
+    pre_s = sum(p for p, _ in timed)
+    value = len(timed) * n_dec / dec_s
+    sample = (f"{wl.name}: prefill of the {wl.n_prompt}-position prompt + {n_dec} greedy decode steps per step "
+              f"(of the workload's {wl.n_decode}), float64 numpy oracle")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * (dec_s + pre_s) / len(timed),
+            "ms_per_token": 1e3 * dec_s / (len(timed) * n_dec),
+            "prefill_tok_s": len(timed) * wl.n_prompt / pre_s, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": workload_desc(wl),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    from qwen3_prefill_kv_gb300 import synth, build
+    from qwen3_prefill_kv_gb300 import _lib
+    build.build()
+    _lib.load()
+    wl = synth.WORKLOADS[args.workload]
+    shape = wl.shape
+    dev = torch.device("cuda", local_rank)
+    w = synth.make_weights(shape, seed=0).to(dev)
+    prompt = synth.make_prompt(wl, seed=rank)
+    ids = prompt.ids
+    audio_dev = prompt.audio.to(dev)
+    stream = torch.cuda.Stream(device=dev)
+    dec = _lib.Decoder(shape, w, max_seq=wl.max_seq, stream=stream)
+
+    def step_device(ev_mid=None):
+        dec.prefill(ids, audio_dev, prompt.audio_offset, want_argmax=False)
+        if ev_mid is not None:
+            ev_mid.record(stream)
+        for _ in range(wl.n_decode):
+            dec.decode_step(-1, want_argmax=False)
+
+    # warm-up (includes the one-time capture of the decode graph)
+    for _ in range(args.warmup):
+        step_device()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    launches0 = _lib.kernel_launches()
+    with ClockSampler(torch.cuda.current_device() if world == 1 else local_rank) as clk:
+        torch.cuda.synchronize(dev)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            step_device(mids[i])
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    launches = _lib.kernel_launches() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    pre_ms = [s.elapsed_time(m) for s, m in zip(starts, mids)]
+    dec_ms = [m.elapsed_time(e) for m, e in zip(mids, ends)]
+    tot_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    clocks = clk.summary()
+
+    # e2e through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        ids_h = ids.clone().pin_memory()
+        audio_h = prompt.audio.clone().pin_memory()
+        logits_h = torch.empty(shape.vocab, dtype=torch.float32).pin_memory()
+        def step_host():
+            tok = dec.prefill(ids_h, audio_h, prompt.audio_offset)
+            for j in range(wl.n_decode):
+                last = j == wl.n_decode - 1
+                tok = dec.decode_step(tok, logits=logits_h if last else None)
+            return tok
+        for _ in range(max(1, args.warmup)):
+            step_host()
+        torch.cuda.synchronize(dev)
+        e_dec = []
+        for _ in range(args.steps):
+            t0 = time.perf_counter()
+            tok = dec.prefill(ids_h, audio_h, prompt.audio_offset)
+            t1 = time.perf_counter()
+            for j in range(wl.n_decode):
+                last = j == wl.n_decode - 1
+                tok = dec.decode_step(tok, logits=logits_h if last else None)
+            torch.cuda.synchronize(dev)
+            e_dec.append(time.perf_counter() - t1)
+        h2d = ids.numel() * 4 + prompt.audio.numel() * 2 + wl.n_decode * 4
+        d2h = (wl.n_decode + 1) * 4 + shape.vocab * 4
+        e2e_val = wl.n_decode * len(e_dec) / sum(e_dec)
+        e2e = {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_token": 1e3 * sum(e_dec) / (wl.n_decode * len(e_dec))}
+
+    dec_total_s = sum(dec_ms) / 1e3
+    pre_total_s = sum(pre_ms) / 1e3
+    if world > 1:
+        t = torch.tensor([dec_total_s, pre_total_s, sum(tot_ms)], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dec_total_s, pre_total_s, tot = t.tolist()
+        tot_ms_mean = tot / args.steps
+    else:
+        tot_ms_mean = sum(tot_ms) / args.steps
+    value = world * wl.n_decode * args.steps / dec_total_s
+    hbm, bf16, peak_kind = peaks()
+    # roofline of the decode step (the dominant part of the step): algorithmic bytes per
+    # step averaged over the KV lengths the timed steps see, over the mean step time.
+    Ls = range(wl.n_prompt + 1, wl.n_prompt + wl.n_decode + 1)
+    bytes_per_token = sum(decode_step_bytes(shape, L) for L in Ls) / len(Ls)
+    t_tok = dec_total_s / (wl.n_decode * args.steps)
+    achieved = bytes_per_token / t_tok / 1e9
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": tot_ms_mean, "ms_per_token": 1e3 * t_tok,
+            "prefill_tok_s": world * wl.n_prompt * args.steps / pre_total_s,
+            "prefill_ms": 1e3 * pre_total_s / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded random-init bf16 weights of the Qwen3-0.6B shape; seeded ids and audio rows)",
+            "config": dict(workload_desc(wl), parallelism=f"replicas{world}"),
+            "roofline": {"bound": "hbm", "kernel": "decode step (all kernels of one token)",
+                         "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "peak_kind": peak_kind, "traffic": None,
+                         "algorithmic_bytes_per_launch": bytes_per_token},
+            "clocks": clocks, "gpu_launches": int(launches) * world,
+            "e2e": e2e}
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        try:
+            res, cores = oracle_sample(wl, 4, reps=1)
+            (p_s, d_s), = res
+            line["cpu_baseline"] = {"value": 4 / d_s, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                    "sample": f"{wl.name}: prefill of {wl.n_prompt} positions ({p_s:.2f} s) + 4 "
+                                              f"greedy decode steps ({d_s:.2f} s), float64 numpy oracle"}
+        except Exception as e:  # pragma: no cover
+            line["cpu_baseline"] = {"value": None, "unit": UNIT, "cores": None, "kind": "oracle",
+                                    "sample": f"failed: {e}"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    dec.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

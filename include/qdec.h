@@ -1,0 +1,160 @@
+/*
+ * qdec.h — C ABI of a GB300 (sm_103a) library for the Qwen3-0.6B-shape causal
+ * decoder behind the speech-LLM ASR pipelines described in "Forward map -
+ * funasr_nano" (transcribe.cpp), "Qwen3ASR ncnn多平台移植" (ncnn discussion) and
+ * "Fun-ASR-Nano Native Runtime Implementation Plan" (audio.cpp).
+ *
+ * The path: multimodal prefill (token-embedding gather with audio rows spliced
+ * in at an offset), then single-token incremental decode over a per-layer KV
+ * cache, then the tied lm_head with greedy argmax; contexts can be cloned to
+ * branch from one prefill state and stepped together in a batch.
+ *
+ * Conventions shared by every call:
+ *  - All calls return 0 (QDEC_OK) or a negative QDEC_E_* code; nothing throws
+ *    across the ABI.  On an error other than QDEC_E_CUDA the context is left
+ *    unchanged.  qdec_last_error() gives a message for the calling thread.
+ *  - Weights are BORROWED device pointers (bf16, row-major [out, in]) that
+ *    must stay valid for the life of every context created from them,
+ *    clones included.  A context OWNS its KV cache and scratch.
+ *  - Work is queued on the stream given to qdec_create (NULL = a stream the
+ *    context creates).  Calls that return an argmax to the host synchronise
+ *    that stream; calls without host outputs only queue work.
+ *  - Pointers documented as "host or device" are classified with
+ *    cudaPointerGetAttributes: device and managed memory are used in place,
+ *    anything else is copied through a staging buffer.
+ *  - A context is not thread-safe; distinct contexts may be used from
+ *    distinct threads if they use distinct streams.
+ */
+#ifndef QDEC_H
+#define QDEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QDEC_OK              0
+#define QDEC_E_INVALID_ARG  (-1)  /* null pointer, id outside [0, vocab), bad sizes/offsets */
+#define QDEC_E_CAPACITY     (-2)  /* the step would write a KV slot >= max_seq */
+#define QDEC_E_STATE        (-3)  /* decode before prefill, mixed contexts in a batch */
+#define QDEC_E_CUDA         (-4)  /* a CUDA runtime/driver call failed (context may be unusable) */
+#define QDEC_E_OOM          (-5)  /* device or pinned allocation failed */
+#define QDEC_E_TIMEOUT      (-6)  /* a bounded device-side wait gave up (error flag set by a kernel) */
+#define QDEC_E_UNSUPPORTED  (-7)  /* model shape outside what the kernels implement */
+
+/* Model shape.  Qwen3-0.6B: hidden 1024, 28 layers, 16 q heads, 8 kv heads,
+ * head_dim 128, ffn 3072, vocab 151936, rope_theta 1e6, rms_eps 1e-6
+ * ("Fun-ASR-Nano Native Runtime Implementation Plan", Task 1 Step 1; "Forward
+ * map - funasr_nano", LLM decoder table).  max_seq is the KV-cache capacity
+ * in positions (prompt + generated tokens).
+ * Supported by the kernels: head_dim in {32, 64, 128}; n_q_heads a multiple of
+ * n_kv_heads with at most 8 q heads per kv head; hidden and ffn multiples of
+ * 128; (n_q_heads + 2 n_kv_heads) * head_dim a multiple of 128. */
+typedef struct {
+    int32_t hidden, n_layers, n_q_heads, n_kv_heads, head_dim, ffn, vocab;
+    float   rope_theta, rms_eps;
+    int32_t max_seq;
+} qdec_config;
+
+/* Device pointers to bf16 weights.  Per-layer entries are HOST arrays of
+ * n_layers device pointers (read during qdec_create only).
+ *   embed      [vocab, hidden]   token embedding, also the tied lm_head
+ *   final_norm [hidden]
+ *   wqkv[l]    [(Hq + 2 Hkv) D, hidden]  rows: q heads, then k heads, then v heads
+ *   wo[l]      [hidden, Hq D]
+ *   wgu[l]     [2 ffn, hidden]   rows [0, ffn) gate, [ffn, 2 ffn) up ("packed gate_up")
+ *   wd[l]      [hidden, ffn]
+ *   g_in[l], g_post[l] [hidden];  g_q[l], g_k[l] [head_dim]  RMSNorm gains
+ * Every pointer must be 16-byte aligned. */
+typedef struct {
+    const void *embed;
+    const void *final_norm;
+    const void *const *wqkv, *const *wo, *const *wgu, *const *wd;
+    const void *const *g_in, *const *g_post, *const *g_q, *const *g_k;
+} qdec_weights;
+
+typedef struct qdec_ctx qdec_ctx;
+
+/* Creates a context: validates the shape, records the weight pointers,
+ * allocates the KV cache [n_layers][2][n_kv_heads][max_seq][head_dim] bf16,
+ * the decode scratch and a RoPE cos/sin table [max_seq][head_dim/2] (angles
+ * p * theta^(-2i/D) evaluated in double on the host, stored as fp32).
+ * `cuda_stream` is a cudaStream_t or NULL.  *out receives the context. */
+int qdec_create(const qdec_config *cfg, const qdec_weights *w, void *cuda_stream, qdec_ctx **out);
+
+/* Prefill ("Forward map - funasr_nano", Generation / KV Path, "Prefill, all
+ * positions"; "Qwen3ASR ncnn多平台移植" §4-§5).  Resets the context to position
+ * 0, embeds ids[0..n_ids) (HOST int32), overrides rows [audio_offset,
+ * audio_offset + n_audio) with audio_rows (bf16 [n_audio, hidden], host or
+ * device; the ids under them are range-checked and otherwise ignored), runs
+ * all layers writing KV slots [0, n_ids), and evaluates the tied lm_head on
+ * the LAST position only.
+ *   logits_out: NULL or fp32 [vocab], host or device.
+ *   argmax_out: NULL or HOST int32; lowest index among equal maxima.
+ * Synchronises the stream only when argmax_out is given.
+ * Errors: INVALID_ARG (n_ids <= 0, id out of range, audio range outside the
+ * prompt, n_audio > 0 with NULL rows), CAPACITY (n_ids > max_seq). */
+int qdec_prefill(qdec_ctx *ctx, const int32_t *ids, int32_t n_ids,
+                 const void *audio_rows, int32_t n_audio, int32_t audio_offset,
+                 float *logits_out, int32_t *argmax_out);
+
+/* One incremental decode step at position n = qdec_position(ctx)
+ * ("Qwen3ASR ncnn多平台移植" §5 steps 1-6; "Forward map - funasr_nano",
+ * "Single-step decode @ n_past >= T_prompt").  token >= 0 is embedded; token
+ * == -1 feeds back the previous step's argmax without a host round trip.
+ * Writes KV slot n, advances the position by one, evaluates the lm_head.
+ * logits_out / argmax_out as in qdec_prefill.  Errors: STATE (no prefill),
+ * CAPACITY (n >= max_seq), INVALID_ARG (token < -1 or >= vocab). */
+int qdec_decode_step(qdec_ctx *ctx, int32_t token, float *logits_out, int32_t *argmax_out);
+
+/* One lockstep decode step for n contexts (clones of one prefill or
+ * independent prompts) sharing weights and shape.  tokens: HOST int32 [n]
+ * (-1 = previous argmax of that context).  logits_out: NULL or fp32
+ * [n, vocab] (host or device); argmax_out: NULL or HOST int32 [n].  Each
+ * context advances by one.  Errors as qdec_decode_step, plus STATE when the
+ * contexts were not created from the same weights and shape. */
+int qdec_decode_step_batch(qdec_ctx *const *ctxs, int32_t n, const int32_t *tokens,
+                           float *logits_out, int32_t *argmax_out);
+
+/* Deep copy of a context ("Qwen3ASR ncnn多平台移植" §5: generation clones its
+ * input context so several branches can start from one prefill state): KV
+ * slots [0, position), token history, position and last argmax.  Weights are
+ * shared; the clone gets its own scratch and uses the source's stream. */
+int qdec_clone(const qdec_ctx *src, qdec_ctx **out);
+
+/* Number of positions written (prompt + decoded tokens); 0 before prefill;
+ * a negative code for a NULL context. */
+int qdec_position(const qdec_ctx *ctx);
+
+/* Copies KV slots [pos0, pos0 + n_pos) of one layer to HOST memory as bf16
+ * [n_kv_heads][n_pos][head_dim].  kind 0 = K (after Q/K-norm and RoPE),
+ * 1 = V.  Synchronises the stream. */
+int qdec_read_kv(const qdec_ctx *ctx, int32_t layer, int32_t kind, int32_t pos0, int32_t n_pos,
+                 void *host_dst);
+
+/* Copies the token history [0, position) (prompt ids, then each decode
+ * step's input token) to HOST int32.  Synchronises the stream. */
+int qdec_read_history(const qdec_ctx *ctx, int32_t *host_dst, int32_t n);
+
+/* Waits for all work queued by this context. */
+int qdec_sync(const qdec_ctx *ctx);
+
+/* Frees the context (KV cache, scratch, graphs).  NULL is a no-op. */
+void qdec_destroy(qdec_ctx *ctx);
+
+/* Static description of a status code. */
+const char *qdec_strerror(int status);
+
+/* Message of the most recent failure on the calling thread ("" if none). */
+const char *qdec_last_error(void);
+
+/* Number of kernels this library has launched in the process so far (a CUDA
+ * graph replay counts its kernel nodes).  A diagnostic for benchmarks. */
+uint64_t qdec_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QDEC_H */

@@ -1,0 +1,60 @@
+/*
+ * qdec_ops.h — per-kernel entry points of the qdec library, for testing one
+ * step of the decoder path in isolation.  All pointers are DEVICE pointers
+ * unless stated; work is queued on `stream` (a cudaStream_t, NULL = legacy
+ * default stream) and nothing is synchronised.  Return 0 or a QDEC_E_* code
+ * (include/qdec.h); a launch failure returns QDEC_E_CUDA.
+ */
+#ifndef QDEC_OPS_H
+#define QDEC_OPS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QDEC_GEMM_STORE_F32   0   /* C[m,n] = acc                               (fp32 C) */
+#define QDEC_GEMM_ADD_F32     1   /* C[m,n] += acc   (residual add)             (fp32 C) */
+#define QDEC_GEMM_SWIGLU_BF16 2   /* C[m,n] = silu(gate) * up, W = [gate rows; up rows at up_off] (bf16 C) */
+#define QDEC_GEMM_STORE_BF16  3   /* C[m,n] = bf16(acc)                         (bf16 C) */
+
+#define QDEC_IMPL_SIMT     0      /* CUDA-core kernel */
+#define QDEC_IMPL_TCGEN05  1      /* tcgen05 / TMEM / TMA kernel */
+
+/* C[M, N] = A[M, K] . W[N, K]^T with bf16 A (row stride lda elements) and W
+ * (row-major, K contiguous), fp32 accumulation, and the epilogue `mode`
+ * ("Forward map - funasr_nano", LLM decoder table: the block's projections,
+ * residual adds and packed gate_up SwiGLU).  ldc is C's row stride in
+ * elements.  Shape limits: K % 64 == 0 for TCGEN05, K % 32 == 0 for SIMT. */
+int qdec_op_gemm(const void *A, int32_t lda, const void *W, int32_t M, int32_t N, int32_t K, int32_t mode,
+                 int32_t up_off, void *C, int32_t ldc, int32_t impl, void *stream);
+
+/* Causal GQA attention for T query rows at positions pos0..pos0+T-1 over
+ * cache keys [0, pos0 + T): Q bf16 [T, HQ, D]; k_cache / v_cache bf16
+ * [HKV][max_seq][D]; O bf16 [T, HQ * D] ("Qwen3ASR ncnn多平台移植" §5, the
+ * prefill's upper-triangular causal mask; GQA 16/8 in the forward map). */
+int qdec_op_attention_prefill(const void *Q, int32_t T, int32_t HQ, int32_t HKV, int32_t D, int32_t max_seq,
+                              int32_t pos0, const void *k_cache, const void *v_cache, void *O, int32_t impl,
+                              void *stream);
+
+/* Bytes of scratch qdec_op_lm_head_argmax needs for a vocabulary of V rows. */
+size_t qdec_op_lm_head_scratch_bytes(int32_t V);
+
+/* Tied lm_head with the final RMSNorm fused in front ("Forward map -
+ * funasr_nano": `rms_norm * w` then `mul_mat(token_w, last_x)`):
+ * h = x * rsqrt(mean x^2 + eps) * g_final, logits[v] = E[v] . h (fp32 [V]),
+ * *argmax = lowest index among the maximal logits (device int32).
+ * x fp32 [H]; E bf16 [V, H]; g_final bf16 [H].  `scratch` (caller-owned,
+ * >= qdec_op_lm_head_scratch_bytes(V)) holds per-block partial maxima and a
+ * ticket counter whose first 4 bytes must be zero before the first call;
+ * every call leaves them zero again.  Calls sharing a scratch must not
+ * overlap on the GPU. */
+int qdec_op_lm_head_argmax(const void *E, int32_t V, int32_t H, const float *x, const void *g_final, float eps,
+                           float *logits, int32_t *argmax, void *scratch, size_t scratch_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QDEC_OPS_H */

@@ -1,0 +1,222 @@
+"""ctypes binding of the qdec C ABI (include/qdec.h, include/qdec_ops.h).
+
+Argument marshalling only: every step of the decoder runs in the CUDA library.
+There is no CPU fallback: if libqdec.so is missing, loading raises.
+PyTorch tensors are accepted for buffers (their data_ptr is passed through).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libqdec.so")
+
+QDEC_OK = 0
+STATUS = {-1: "INVALID_ARG", -2: "CAPACITY", -3: "STATE", -4: "CUDA", -5: "OOM", -6: "TIMEOUT",
+          -7: "UNSUPPORTED"}
+
+GEMM_STORE_F32, GEMM_ADD_F32, GEMM_SWIGLU_BF16, GEMM_STORE_BF16 = 0, 1, 2, 3
+IMPL_SIMT, IMPL_TCGEN05 = 0, 1
+
+
+class QdecError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class QdecConfig(C.Structure):
+    _fields_ = [("hidden", C.c_int32), ("n_layers", C.c_int32), ("n_q_heads", C.c_int32),
+                ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("ffn", C.c_int32),
+                ("vocab", C.c_int32), ("rope_theta", C.c_float), ("rms_eps", C.c_float),
+                ("max_seq", C.c_int32)]
+
+
+_PP = C.POINTER(C.c_void_p)
+
+
+class QdecWeights(C.Structure):
+    _fields_ = [("embed", C.c_void_p), ("final_norm", C.c_void_p), ("wqkv", _PP), ("wo", _PP),
+                ("wgu", _PP), ("wd", _PP), ("g_in", _PP), ("g_post", _PP), ("g_q", _PP), ("g_k", _PP)]
+
+
+_lib = None
+
+# Every symbol include/qdec.h and include/qdec_ops.h declare: (name, restype, argtypes).
+_VP, _I32, _F, _SZ = C.c_void_p, C.c_int32, C.c_float, C.c_size_t
+SIGNATURES = [
+    ("qdec_create", C.c_int, [C.POINTER(QdecConfig), C.POINTER(QdecWeights), _VP, C.POINTER(_VP)]),
+    ("qdec_prefill", C.c_int, [_VP, _VP, _I32, _VP, _I32, _I32, _VP, _VP]),
+    ("qdec_decode_step", C.c_int, [_VP, _I32, _VP, _VP]),
+    ("qdec_decode_step_batch", C.c_int, [_VP, _I32, _VP, _VP, _VP]),
+    ("qdec_clone", C.c_int, [_VP, C.POINTER(_VP)]),
+    ("qdec_position", C.c_int, [_VP]),
+    ("qdec_read_kv", C.c_int, [_VP, _I32, _I32, _I32, _I32, _VP]),
+    ("qdec_read_history", C.c_int, [_VP, _VP, _I32]),
+    ("qdec_sync", C.c_int, [_VP]),
+    ("qdec_destroy", None, [_VP]),
+    ("qdec_strerror", C.c_char_p, [C.c_int]),
+    ("qdec_last_error", C.c_char_p, []),
+    ("qdec_kernel_launches", C.c_uint64, []),
+    ("qdec_op_gemm", C.c_int, [_VP, _I32, _VP, _I32, _I32, _I32, _I32, _I32, _VP, _I32, _I32, _VP]),
+    ("qdec_op_attention_prefill", C.c_int, [_VP, _I32, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _I32, _VP]),
+    ("qdec_op_lm_head_scratch_bytes", _SZ, [_I32]),
+    ("qdec_op_lm_head_argmax", C.c_int, [_VP, _I32, _I32, _VP, _VP, _F, _VP, _VP, _VP, _SZ, _VP]),
+]
+
+
+def load(path: str = LIB_PATH):
+    """Loads libqdec.so (built by ``qwen3_prefill_kv_gb300.build``); raises if it is absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with `python -m qwen3_prefill_kv_gb300.build` "
+                          "(the decoder has no CPU fallback)")
+    lib = C.CDLL(path)
+    for name, res, args in SIGNATURES:
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(rc: int) -> None:
+    if rc != QDEC_OK:
+        raise QdecError(rc, (_lib.qdec_last_error() or b"").decode())
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    return t.data_ptr()
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        return None
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+class Decoder:
+    """One decoding context (KV cache + state) over borrowed device weights.
+
+    ``weights`` is a ``synth.Weights`` (or any object with the same fields)
+    whose tensors live on the GPU; the object is kept alive by the Decoder."""
+
+    def __init__(self, shape, weights, max_seq: int, stream=None, _handle=None):
+        self.lib = load()
+        self.shape = shape
+        self.weights = weights
+        self.max_seq = max_seq
+        self._stream = stream
+        if _handle is not None:
+            self.handle = _handle
+            return
+        cfg = QdecConfig(shape.hidden, shape.n_layers, shape.n_q_heads, shape.n_kv_heads, shape.head_dim,
+                         shape.ffn, shape.vocab, shape.rope_theta, shape.rms_eps, max_seq)
+        nl = shape.n_layers
+        arrs = {}
+        for k in ("wqkv", "wo", "wgu", "wd", "g_in", "g_post", "g_q", "g_k"):
+            arrs[k] = (C.c_void_p * nl)(*[l[k].data_ptr() for l in weights.layers])
+        self._arrs = arrs
+        w = QdecWeights(weights.embed.data_ptr(), weights.final_norm.data_ptr(),
+                        *[C.cast(arrs[k], _PP) for k in ("wqkv", "wo", "wgu", "wd", "g_in", "g_post", "g_q", "g_k")])
+        h = C.c_void_p()
+        _check(self.lib.qdec_create(C.byref(cfg), C.byref(w), _stream_handle(stream), C.byref(h)))
+        self.handle = h
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            self.lib.qdec_destroy(self.handle)
+            self.handle = None
+
+    __del__ = close
+
+    @property
+    def position(self) -> int:
+        r = self.lib.qdec_position(self.handle)
+        if r < 0:
+            _check(r)
+        return r
+
+    def prefill(self, ids, audio=None, audio_offset: int = 0, logits=None, want_argmax: bool = True):
+        ids_np = np.ascontiguousarray(np.asarray(ids if not hasattr(ids, "numpy") else ids.cpu().numpy(),
+                                                 dtype=np.int32))
+        n_audio = 0 if audio is None else int(audio.shape[0])
+        out = np.zeros(1, dtype=np.int32)
+        _check(self.lib.qdec_prefill(self.handle, _ptr(ids_np), int(ids_np.size), _ptr(audio), n_audio,
+                                     int(audio_offset), _ptr(logits), _ptr(out) if want_argmax else None))
+        return int(out[0]) if want_argmax else None
+
+    def decode_step(self, token: int = -1, logits=None, want_argmax: bool = True):
+        out = np.zeros(1, dtype=np.int32)
+        _check(self.lib.qdec_decode_step(self.handle, int(token), _ptr(logits), _ptr(out) if want_argmax else None))
+        return int(out[0]) if want_argmax else None
+
+    def clone(self) -> "Decoder":
+        h = C.c_void_p()
+        _check(self.lib.qdec_clone(self.handle, C.byref(h)))
+        return Decoder(self.shape, self.weights, self.max_seq, self._stream, _handle=h)
+
+    @staticmethod
+    def decode_step_batch(decoders: Sequence["Decoder"], tokens, logits=None, want_argmax: bool = True):
+        n = len(decoders)
+        lib = decoders[0].lib
+        hs = (C.c_void_p * n)(*[d.handle.value if isinstance(d.handle, C.c_void_p) else d.handle for d in decoders])
+        toks = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        out = np.zeros(n, dtype=np.int32)
+        _check(lib.qdec_decode_step_batch(C.cast(hs, C.c_void_p), n, _ptr(toks), _ptr(logits),
+                                          _ptr(out) if want_argmax else None))
+        return out if want_argmax else None
+
+    def read_kv(self, layer: int, kind: int, pos0: int, n_pos: int) -> np.ndarray:
+        """bf16 bits (uint16) [n_kv_heads, n_pos, head_dim] of one layer's K (kind 0) or V (kind 1)."""
+        out = np.zeros((self.shape.n_kv_heads, n_pos, self.shape.head_dim), dtype=np.uint16)
+        _check(self.lib.qdec_read_kv(self.handle, layer, kind, pos0, n_pos, _ptr(out)))
+        return out
+
+    def read_history(self, n: Optional[int] = None) -> np.ndarray:
+        n = self.position if n is None else n
+        out = np.zeros(n, dtype=np.int32)
+        _check(self.lib.qdec_read_history(self.handle, _ptr(out), n))
+        return out
+
+    def sync(self) -> None:
+        _check(self.lib.qdec_sync(self.handle))
+
+
+def kernel_launches() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(load().qdec_kernel_launches())
+
+
+# ------------------------------------------------------------------ per-kernel entry points
+def gemm(A, W, M, N, K, mode, C_out, lda=None, ldc=None, up_off=0, impl=IMPL_SIMT, stream=None) -> None:
+    lib = load()
+    _check(lib.qdec_op_gemm(_ptr(A), lda if lda is not None else K, _ptr(W), M, N, K, mode, up_off, _ptr(C_out),
+                            ldc if ldc is not None else N, impl, _stream_handle(stream)))
+
+
+def attention_prefill(Q, T, HQ, HKV, D, max_seq, pos0, k_cache, v_cache, O, impl=IMPL_SIMT, stream=None) -> None:
+    lib = load()
+    _check(lib.qdec_op_attention_prefill(_ptr(Q), T, HQ, HKV, D, max_seq, pos0, _ptr(k_cache), _ptr(v_cache),
+                                         _ptr(O), impl, _stream_handle(stream)))
+
+
+def lm_head_scratch_bytes(V: int) -> int:
+    return int(load().qdec_op_lm_head_scratch_bytes(V))
+
+
+def lm_head_argmax(E, V, H, x, g_final, eps, logits, argmax, scratch, stream=None) -> None:
+    lib = load()
+    nbytes = scratch.numel() * scratch.element_size()
+    _check(lib.qdec_op_lm_head_argmax(_ptr(E), V, H, _ptr(x), _ptr(g_final), float(eps), _ptr(logits),
+                                      _ptr(argmax), _ptr(scratch), nbytes, _stream_handle(stream)))

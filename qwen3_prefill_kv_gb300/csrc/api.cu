@@ -1,0 +1,586 @@
+// C ABI (include/qdec.h): context lifetime, argument validation, host/device buffer
+// handling, and the prefill / decode / clone orchestration of the kernels.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/qdec.h"
+#include "common.cuh"
+
+using namespace qdec;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+#define CK(call)                                                                                   \
+    do {                                                                                           \
+        cudaError_t e_ = (call);                                                                   \
+        if (e_ != cudaSuccess)                                                                     \
+            return fail(e_ == cudaErrorMemoryAllocation ? QDEC_E_OOM : QDEC_E_CUDA, "%s: %s (%s:%d)", \
+                        #call, cudaGetErrorString(e_), __FILE__, __LINE__);                        \
+    } while (0)
+
+bool is_device_ptr(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct LayerW {
+    const bf16_t *wqkv, *wo, *wgu, *wd, *g_in, *g_post, *g_q, *g_k;
+};
+
+}  // namespace
+
+namespace qdec {
+static unsigned long long g_launches = 0;
+void count_launches(uint64_t n) { __atomic_fetch_add(&g_launches, (unsigned long long)n, __ATOMIC_RELAXED); }
+}  // namespace qdec
+
+struct qdec_ctx {
+    qdec_config cfg;
+    Shape sh;
+    const bf16_t* embed = nullptr;
+    const bf16_t* final_norm = nullptr;
+    std::vector<LayerW> layers;
+    cudaStream_t stream = nullptr;
+    bool own_stream = false;
+    cudaStream_t cap_stream = nullptr;   // internal stream used only for graph capture
+    int device = 0;
+
+    int position = 0;
+    bool prefilled = false;
+
+    // persistent device state
+    bf16_t* kv = nullptr;        // [NL][2][HKV][max_seq][D]
+    float2* rope = nullptr;      // [max_seq][D/2] (cos, sin)
+    int* d_hist = nullptr;       // [max_seq]
+    int* d_pos = nullptr;        // position of the next token
+    int* d_zero = nullptr;       // constant 0 (prefill start position)
+    int* d_argmax = nullptr;
+
+    // decode scratch
+    float *d_x = nullptr, *d_qkv = nullptr, *d_q = nullptr, *d_attn = nullptr, *d_h = nullptr;
+    float *d_logits = nullptr, *d_part_ml = nullptr, *d_part_o = nullptr;
+    void* d_lm_scratch = nullptr;
+    int n_split = 1;
+
+    // prefill scratch (grown on demand)
+    int pf_cap = 0;
+    float *p_X = nullptr, *p_qkv = nullptr;
+    bf16_t *p_Xn = nullptr, *p_Q = nullptr, *p_O = nullptr, *p_H = nullptr;
+    int* p_ids = nullptr;
+    int audio_cap = 0;
+    bf16_t* p_audio = nullptr;
+
+    int* h_pinned = nullptr;     // pinned host staging (argmax values)
+    int h_pinned_cap = 0;
+
+    cudaGraphExec_t decode_exec = nullptr;
+    uint64_t decode_graph_kernels = 0;   // kernel nodes in decode_exec
+
+    size_t kv_layer_stride() const { return (size_t)2 * sh.HKV * sh.max_seq * sh.D; }
+    bf16_t* k_cache(int l) { return kv + (size_t)l * kv_layer_stride(); }
+    bf16_t* v_cache(int l) { return kv + (size_t)l * kv_layer_stride() + (size_t)sh.HKV * sh.max_seq * sh.D; }
+};
+
+namespace {
+
+template <typename T>
+cudaError_t dalloc(T** p, size_t n) {
+    return cudaMalloc(reinterpret_cast<void**>(p), n * sizeof(T) > 0 ? n * sizeof(T) : 16);
+}
+
+void free_all(qdec_ctx* c) {
+    if (c->decode_exec) cudaGraphExecDestroy(c->decode_exec);
+    void* ptrs[] = {c->kv, c->rope, c->d_hist, c->d_pos, c->d_zero, c->d_argmax, c->d_x, c->d_qkv, c->d_q,
+                    c->d_attn, c->d_h, c->d_logits, c->d_part_ml, c->d_part_o, c->d_lm_scratch, c->p_X,
+                    c->p_qkv, c->p_Xn, c->p_Q, c->p_O, c->p_H, c->p_ids, c->p_audio};
+    for (void* p : ptrs)
+        if (p) cudaFree(p);
+    if (c->h_pinned) cudaFreeHost(c->h_pinned);
+    if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
+    if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
+}
+
+int validate_config(const qdec_config* c) {
+    if (c->hidden <= 0 || c->n_layers <= 0 || c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0 ||
+        c->ffn <= 0 || c->vocab <= 0 || c->max_seq <= 0)
+        return fail(QDEC_E_INVALID_ARG, "non-positive dimension in qdec_config");
+    if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f))
+        return fail(QDEC_E_INVALID_ARG, "rms_eps and rope_theta must be positive");
+    if (c->head_dim != 32 && c->head_dim != 64 && c->head_dim != 128)
+        return fail(QDEC_E_UNSUPPORTED, "head_dim %d not in {32, 64, 128}", c->head_dim);
+    if (c->n_q_heads % c->n_kv_heads != 0)
+        return fail(QDEC_E_UNSUPPORTED, "n_q_heads must be a multiple of n_kv_heads");
+    const int g = c->n_q_heads / c->n_kv_heads;
+    if (g != 1 && g != 2 && g != 4 && g != 8)
+        return fail(QDEC_E_UNSUPPORTED, "q heads per kv head (%d) not in {1, 2, 4, 8}", g);
+    if (c->hidden % 128 != 0 || c->ffn % 128 != 0)
+        return fail(QDEC_E_UNSUPPORTED, "hidden and ffn must be multiples of 128");
+    if (((c->n_q_heads + 2 * c->n_kv_heads) * c->head_dim) % 128 != 0)
+        return fail(QDEC_E_UNSUPPORTED, "(n_q_heads + 2 n_kv_heads) * head_dim must be a multiple of 128");
+    if ((c->n_q_heads * c->head_dim) % 128 != 0)
+        return fail(QDEC_E_UNSUPPORTED, "n_q_heads * head_dim must be a multiple of 128");
+    return QDEC_OK;
+}
+
+int alloc_state(qdec_ctx* c) {
+    const Shape& sh = c->sh;
+    CK(cudaGetDevice(&c->device));
+    CK(cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking));
+    CK(dalloc(&c->kv, (size_t)sh.NL * c->kv_layer_stride()));
+    CK(cudaMemset(c->kv, 0, (size_t)sh.NL * c->kv_layer_stride() * sizeof(bf16_t)));
+    CK(dalloc(&c->rope, (size_t)sh.max_seq * (sh.D / 2)));
+    CK(dalloc(&c->d_hist, (size_t)sh.max_seq));
+    CK(dalloc(&c->d_pos, 1));
+    CK(dalloc(&c->d_zero, 1));
+    CK(dalloc(&c->d_argmax, 1));
+    CK(cudaMemset(c->d_pos, 0, sizeof(int)));
+    CK(cudaMemset(c->d_zero, 0, sizeof(int)));
+    CK(cudaMemset(c->d_argmax, 0, sizeof(int)));
+    CK(dalloc(&c->d_x, sh.H));
+    CK(dalloc(&c->d_qkv, sh.qkv_rows()));
+    CK(dalloc(&c->d_q, (size_t)sh.HQ * sh.D));
+    CK(dalloc(&c->d_attn, (size_t)sh.HQ * sh.D));
+    CK(dalloc(&c->d_h, sh.F));
+    CK(dalloc(&c->d_logits, sh.V));
+    c->n_split = attention_decode_splits(sh);
+    CK(dalloc(&c->d_part_ml, (size_t)sh.HQ * c->n_split * 2));
+    CK(dalloc(&c->d_part_o, (size_t)sh.HQ * c->n_split * sh.D));
+    const size_t lm = lm_head_scratch_bytes(sh.V);
+    CK(cudaMalloc(&c->d_lm_scratch, lm));
+    CK(cudaMemset(c->d_lm_scratch, 0, lm));
+    CK(cudaMallocHost(reinterpret_cast<void**>(&c->h_pinned), 64 * sizeof(int)));
+    c->h_pinned_cap = 64;
+    return QDEC_OK;
+}
+
+int build_rope_table(qdec_ctx* c) {
+    const int half = c->sh.D / 2;
+    std::vector<float2> t((size_t)c->sh.max_seq * half);
+    for (int p = 0; p < c->sh.max_seq; ++p)
+        for (int i = 0; i < half; ++i) {
+            const double inv = std::pow((double)c->cfg.rope_theta, -2.0 * i / (double)c->sh.D);
+            const double a = (double)p * inv;
+            t[(size_t)p * half + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+        }
+    CK(cudaMemcpy(c->rope, t.data(), t.size() * sizeof(float2), cudaMemcpyHostToDevice));
+    return QDEC_OK;
+}
+
+int ensure_prefill_scratch(qdec_ctx* c, int T) {
+    if (T <= c->pf_cap) return QDEC_OK;
+    const Shape& sh = c->sh;
+    void* old[] = {c->p_X, c->p_qkv, c->p_Xn, c->p_Q, c->p_O, c->p_H, c->p_ids};
+    CK(cudaStreamSynchronize(c->stream));
+    for (void* p : old)
+        if (p) cudaFree(p);
+    c->p_X = c->p_qkv = nullptr;
+    c->p_Xn = c->p_Q = c->p_O = c->p_H = nullptr;
+    c->p_ids = nullptr;
+    c->pf_cap = 0;
+    CK(dalloc(&c->p_X, (size_t)T * sh.H));
+    CK(dalloc(&c->p_qkv, (size_t)T * sh.qkv_rows()));
+    CK(dalloc(&c->p_Xn, (size_t)T * sh.H));
+    CK(dalloc(&c->p_Q, (size_t)T * sh.HQ * sh.D));
+    CK(dalloc(&c->p_O, (size_t)T * sh.HQ * sh.D));
+    CK(dalloc(&c->p_H, (size_t)T * sh.F));
+    CK(dalloc(&c->p_ids, (size_t)T));
+    c->pf_cap = T;
+    return QDEC_OK;
+}
+
+int ensure_audio_staging(qdec_ctx* c, int n) {
+    if (n <= c->audio_cap) return QDEC_OK;
+    CK(cudaStreamSynchronize(c->stream));
+    if (c->p_audio) cudaFree(c->p_audio);
+    c->p_audio = nullptr;
+    c->audio_cap = 0;
+    CK(dalloc(&c->p_audio, (size_t)n * c->sh.H));
+    c->audio_cap = n;
+    return QDEC_OK;
+}
+
+int ensure_pinned(qdec_ctx* c, int n) {
+    if (n <= c->h_pinned_cap) return QDEC_OK;
+    CK(cudaStreamSynchronize(c->stream));
+    cudaFreeHost(c->h_pinned);
+    c->h_pinned = nullptr;
+    c->h_pinned_cap = 0;
+    CK(cudaMallocHost(reinterpret_cast<void**>(&c->h_pinned), (size_t)n * sizeof(int)));
+    c->h_pinned_cap = n;
+    return QDEC_OK;
+}
+
+// Copies the step's logits to the caller (host or device) on the context's stream.
+int copy_logits_out(qdec_ctx* c, float* dst) {
+    if (!dst) return QDEC_OK;
+    CK(cudaMemcpyAsync(dst, c->d_logits, (size_t)c->sh.V * sizeof(float), cudaMemcpyDefault, c->stream));
+    return QDEC_OK;
+}
+
+constexpr uint64_t kPrefillKernelsPerLayer = 8;
+
+// One layer of the prefill over T rows starting at position 0.
+int prefill_layer(qdec_ctx* c, int l, int T) {
+    const Shape& sh = c->sh;
+    const LayerW& w = c->layers[l];
+    cudaStream_t s = c->stream;
+    const int qd = sh.HQ * sh.D;
+    CK(launch_rmsnorm_bf16(c->p_X, T, sh.H, w.g_in, sh.eps, c->p_Xn, s));
+    CK(launch_gemm_simt(c->p_Xn, sh.H, w.wqkv, T, sh.qkv_rows(), sh.H, GEMM_STORE_F32, 0, c->p_qkv, nullptr,
+                        sh.qkv_rows(), s));
+    CK(launch_qk_norm_rope_append(c->p_qkv, T, sh, c->d_zero, w.g_q, w.g_k, c->rope, c->p_Q, nullptr,
+                                  c->k_cache(l), c->v_cache(l), s));
+    CK(launch_attention_prefill_simt(c->p_Q, T, sh, 0, c->k_cache(l), c->v_cache(l), c->p_O, s));
+    CK(launch_gemm_simt(c->p_O, qd, w.wo, T, sh.H, qd, GEMM_ADD_F32, 0, c->p_X, nullptr, sh.H, s));
+    CK(launch_rmsnorm_bf16(c->p_X, T, sh.H, w.g_post, sh.eps, c->p_Xn, s));
+    CK(launch_gemm_simt(c->p_Xn, sh.H, w.wgu, T, sh.F, sh.H, GEMM_SWIGLU_BF16, sh.F, nullptr, c->p_H, sh.F, s));
+    CK(launch_gemm_simt(c->p_H, sh.F, w.wd, T, sh.H, sh.F, GEMM_ADD_F32, 0, c->p_X, nullptr, sh.H, s));
+    return QDEC_OK;
+}
+
+// Queues the decode step body (everything after the token embedding) on stream s.
+int enqueue_decode_body(qdec_ctx* c, cudaStream_t s) {
+    const Shape& sh = c->sh;
+    for (int l = 0; l < sh.NL; ++l) {
+        const LayerW& w = c->layers[l];
+        CK(launch_gemv(w.wqkv, sh.qkv_rows(), sh.H, c->d_x, w.g_in, sh.eps, GEMV_STORE, 0, c->d_qkv, s));
+        CK(launch_qk_norm_rope_append(c->d_qkv, 1, sh, c->d_pos, w.g_q, w.g_k, c->rope, nullptr, c->d_q,
+                                      c->k_cache(l), c->v_cache(l), s));
+        CK(launch_attention_decode(c->d_q, sh, c->d_pos, c->k_cache(l), c->v_cache(l), c->n_split, c->d_part_ml,
+                                   c->d_part_o, c->d_attn, s));
+        CK(launch_gemv(w.wo, sh.H, sh.HQ * sh.D, c->d_attn, nullptr, sh.eps, GEMV_ADD, 0, c->d_x, s));
+        CK(launch_gemv(w.wgu, sh.F, sh.H, c->d_x, w.g_post, sh.eps, GEMV_SWIGLU, sh.F, c->d_h, s));
+        CK(launch_gemv(w.wd, sh.H, sh.F, c->d_h, nullptr, sh.eps, GEMV_ADD, 0, c->d_x, s));
+    }
+    CK(launch_lm_head_argmax(c->embed, sh.V, sh.H, c->d_x, c->final_norm, sh.eps, c->d_logits, c->d_argmax,
+                             c->d_lm_scratch, s));
+    CK(launch_advance_position(c->d_pos, 1, s));
+    return QDEC_OK;
+}
+
+int ensure_decode_graph(qdec_ctx* c) {
+    if (c->decode_exec) return QDEC_OK;
+    cudaGraph_t g = nullptr;
+    CK(cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal));
+    int rc = enqueue_decode_body(c, c->cap_stream);
+    cudaError_t e = cudaStreamEndCapture(c->cap_stream, &g);
+    if (rc != QDEC_OK) {
+        if (g) cudaGraphDestroy(g);
+        return rc;
+    }
+    CK(e);
+    size_t n_nodes = 0;
+    e = cudaGraphGetNodes(g, nullptr, &n_nodes);
+    if (e == cudaSuccess) {
+        std::vector<cudaGraphNode_t> nodes(n_nodes);
+        e = cudaGraphGetNodes(g, nodes.data(), &n_nodes);
+        c->decode_graph_kernels = 0;
+        for (size_t i = 0; e == cudaSuccess && i < n_nodes; ++i) {
+            cudaGraphNodeType t;
+            e = cudaGraphNodeGetType(nodes[i], &t);
+            if (t == cudaGraphNodeTypeKernel) ++c->decode_graph_kernels;
+        }
+    }
+    if (e == cudaSuccess) e = cudaGraphInstantiate(&c->decode_exec, g, 0);
+    cudaGraphDestroy(g);
+    CK(e);
+    return QDEC_OK;
+}
+
+// Queues one decode step (no host synchronisation).
+int enqueue_decode_step(qdec_ctx* c, int token) {
+    int rc = ensure_decode_graph(c);
+    if (rc != QDEC_OK) return rc;
+    CK(launch_embed_token(c->embed, token, c->d_argmax, c->d_pos, c->sh.H, c->d_x, c->d_hist, c->stream));
+    CK(cudaGraphLaunch(c->decode_exec, c->stream));
+    count_launches(1 + c->decode_graph_kernels);
+    return QDEC_OK;
+}
+
+int check_decode_args(const qdec_ctx* c, int token) {
+    if (!c) return fail(QDEC_E_INVALID_ARG, "null context");
+    if (!c->prefilled) return fail(QDEC_E_STATE, "decode before prefill");
+    if (c->position >= c->sh.max_seq)
+        return fail(QDEC_E_CAPACITY, "position %d reached max_seq %d", c->position, c->sh.max_seq);
+    if (token < -1 || token >= c->sh.V) return fail(QDEC_E_INVALID_ARG, "token %d out of range", token);
+    return QDEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qdec_create(const qdec_config* cfg, const qdec_weights* w, void* cuda_stream, qdec_ctx** out) {
+    if (!cfg || !w || !out) return fail(QDEC_E_INVALID_ARG, "null argument");
+    *out = nullptr;
+    int rc = validate_config(cfg);
+    if (rc != QDEC_OK) return rc;
+    if (!w->embed || !w->final_norm || !w->wqkv || !w->wo || !w->wgu || !w->wd || !w->g_in || !w->g_post ||
+        !w->g_q || !w->g_k)
+        return fail(QDEC_E_INVALID_ARG, "null weight pointer");
+    for (int l = 0; l < cfg->n_layers; ++l) {
+        const void* ps[] = {w->wqkv[l], w->wo[l], w->wgu[l], w->wd[l], w->g_in[l], w->g_post[l], w->g_q[l], w->g_k[l]};
+        for (const void* p : ps) {
+            if (!p) return fail(QDEC_E_INVALID_ARG, "null weight pointer in layer %d", l);
+            if (!aligned16(p)) return fail(QDEC_E_INVALID_ARG, "weight pointer of layer %d not 16-byte aligned", l);
+        }
+    }
+    if (!aligned16(w->embed) || !aligned16(w->final_norm))
+        return fail(QDEC_E_INVALID_ARG, "embed / final_norm not 16-byte aligned");
+    qdec_ctx* c = new (std::nothrow) qdec_ctx();
+    if (!c) return fail(QDEC_E_OOM, "host allocation failed");
+    c->cfg = *cfg;
+    c->sh = Shape{cfg->hidden, cfg->n_layers, cfg->n_q_heads, cfg->n_kv_heads, cfg->head_dim, cfg->ffn,
+                  cfg->vocab, cfg->max_seq, cfg->rope_theta, cfg->rms_eps};
+    c->embed = static_cast<const bf16_t*>(w->embed);
+    c->final_norm = static_cast<const bf16_t*>(w->final_norm);
+    c->layers.resize(cfg->n_layers);
+    for (int l = 0; l < cfg->n_layers; ++l)
+        c->layers[l] = LayerW{static_cast<const bf16_t*>(w->wqkv[l]), static_cast<const bf16_t*>(w->wo[l]),
+                              static_cast<const bf16_t*>(w->wgu[l]), static_cast<const bf16_t*>(w->wd[l]),
+                              static_cast<const bf16_t*>(w->g_in[l]), static_cast<const bf16_t*>(w->g_post[l]),
+                              static_cast<const bf16_t*>(w->g_q[l]), static_cast<const bf16_t*>(w->g_k[l])};
+    if (cuda_stream) {
+        c->stream = static_cast<cudaStream_t>(cuda_stream);
+    } else {
+        cudaError_t e = cudaStreamCreateWithFlags(&c->stream, cudaStreamNonBlocking);
+        if (e != cudaSuccess) {
+            delete c;
+            return fail(QDEC_E_CUDA, "cudaStreamCreate: %s", cudaGetErrorString(e));
+        }
+        c->own_stream = true;
+    }
+    rc = alloc_state(c);
+    if (rc == QDEC_OK) rc = build_rope_table(c);
+    if (rc != QDEC_OK) {
+        free_all(c);
+        delete c;
+        return rc;
+    }
+    *out = c;
+    return QDEC_OK;
+}
+
+int qdec_prefill(qdec_ctx* c, const int32_t* ids, int32_t n_ids, const void* audio_rows, int32_t n_audio,
+                 int32_t audio_offset, float* logits_out, int32_t* argmax_out) {
+    if (!c || !ids) return fail(QDEC_E_INVALID_ARG, "null context or ids");
+    if (n_ids <= 0) return fail(QDEC_E_INVALID_ARG, "n_ids must be positive");
+    if (n_ids > c->sh.max_seq) return fail(QDEC_E_CAPACITY, "prompt of %d exceeds max_seq %d", n_ids, c->sh.max_seq);
+    if (n_audio < 0 || audio_offset < 0 || (int64_t)audio_offset + n_audio > n_ids)
+        return fail(QDEC_E_INVALID_ARG, "audio rows [%d, %d) outside the prompt of %d", audio_offset,
+                    audio_offset + n_audio, n_ids);
+    if (n_audio > 0 && !audio_rows) return fail(QDEC_E_INVALID_ARG, "null audio rows");
+    for (int i = 0; i < n_ids; ++i)
+        if (ids[i] < 0 || ids[i] >= c->sh.V) return fail(QDEC_E_INVALID_ARG, "id %d at %d out of range", ids[i], i);
+    const Shape& sh = c->sh;
+    const int T = n_ids;
+    int rc = ensure_prefill_scratch(c, T);
+    if (rc != QDEC_OK) return rc;
+    cudaStream_t s = c->stream;
+    CK(cudaMemcpyAsync(c->p_ids, ids, (size_t)T * sizeof(int), cudaMemcpyHostToDevice, s));
+    const bf16_t* audio = nullptr;
+    if (n_audio > 0) {
+        if (is_device_ptr(audio_rows) && aligned16(audio_rows)) {
+            audio = static_cast<const bf16_t*>(audio_rows);
+        } else {
+            rc = ensure_audio_staging(c, n_audio);
+            if (rc != QDEC_OK) return rc;
+            CK(cudaMemcpyAsync(c->p_audio, audio_rows, (size_t)n_audio * sh.H * sizeof(bf16_t), cudaMemcpyDefault, s));
+            audio = c->p_audio;
+        }
+    }
+    c->prefilled = false;
+    c->position = 0;
+    CK(launch_embed_splice(c->embed, c->p_ids, T, sh.H, audio, n_audio, audio_offset, c->p_X, c->d_hist, s));
+    for (int l = 0; l < sh.NL; ++l) {
+        rc = prefill_layer(c, l, T);
+        if (rc != QDEC_OK) return rc;
+    }
+    CK(launch_lm_head_argmax(c->embed, sh.V, sh.H, c->p_X + (size_t)(T - 1) * sh.H, c->final_norm, sh.eps,
+                             c->d_logits, c->d_argmax, c->d_lm_scratch, s));
+    CK(launch_set_int(c->d_pos, T, s));
+    count_launches(3 + (uint64_t)sh.NL * kPrefillKernelsPerLayer);
+    c->position = T;
+    c->prefilled = true;
+    rc = copy_logits_out(c, logits_out);
+    if (rc != QDEC_OK) return rc;
+    if (argmax_out) {
+        CK(cudaMemcpyAsync(&c->h_pinned[0], c->d_argmax, sizeof(int), cudaMemcpyDeviceToHost, s));
+        CK(cudaStreamSynchronize(s));
+        *argmax_out = c->h_pinned[0];
+    }
+    return QDEC_OK;
+}
+
+int qdec_decode_step(qdec_ctx* c, int32_t token, float* logits_out, int32_t* argmax_out) {
+    int rc = check_decode_args(c, token);
+    if (rc != QDEC_OK) return rc;
+    rc = enqueue_decode_step(c, token);
+    if (rc != QDEC_OK) return rc;
+    c->position += 1;
+    rc = copy_logits_out(c, logits_out);
+    if (rc != QDEC_OK) return rc;
+    if (argmax_out) {
+        CK(cudaMemcpyAsync(&c->h_pinned[0], c->d_argmax, sizeof(int), cudaMemcpyDeviceToHost, c->stream));
+        CK(cudaStreamSynchronize(c->stream));
+        *argmax_out = c->h_pinned[0];
+    }
+    return QDEC_OK;
+}
+
+int qdec_decode_step_batch(qdec_ctx* const* ctxs, int32_t n, const int32_t* tokens, float* logits_out,
+                           int32_t* argmax_out) {
+    if (!ctxs || !tokens || n <= 0) return fail(QDEC_E_INVALID_ARG, "null contexts/tokens or n <= 0");
+    for (int i = 0; i < n; ++i) {
+        int rc = check_decode_args(ctxs[i], tokens[i]);
+        if (rc != QDEC_OK) return rc;
+        if (ctxs[i]->embed != ctxs[0]->embed || memcmp(&ctxs[i]->cfg, &ctxs[0]->cfg, sizeof(qdec_config)) != 0)
+            return fail(QDEC_E_STATE, "batch contexts differ in weights or shape");
+        for (int j = 0; j < i; ++j)
+            if (ctxs[j] == ctxs[i]) return fail(QDEC_E_INVALID_ARG, "context %d repeated in the batch", i);
+    }
+    const int V = ctxs[0]->sh.V;
+    for (int i = 0; i < n; ++i) {
+        qdec_ctx* c = ctxs[i];
+        int rc = enqueue_decode_step(c, tokens[i]);
+        if (rc != QDEC_OK) return rc;
+        c->position += 1;
+        if (logits_out) CK(cudaMemcpyAsync(logits_out + (size_t)i * V, c->d_logits, (size_t)V * sizeof(float),
+                                           cudaMemcpyDefault, c->stream));
+        if (argmax_out)
+            CK(cudaMemcpyAsync(&c->h_pinned[2], c->d_argmax, sizeof(int), cudaMemcpyDeviceToHost, c->stream));
+        if (argmax_out) {
+            CK(cudaStreamSynchronize(c->stream));
+            argmax_out[i] = c->h_pinned[2];
+        }
+    }
+    for (int i = 0; i < n; ++i) CK(cudaStreamSynchronize(ctxs[i]->stream));
+    return QDEC_OK;
+}
+
+int qdec_clone(const qdec_ctx* src, qdec_ctx** out) {
+    if (!src || !out) return fail(QDEC_E_INVALID_ARG, "null argument");
+    *out = nullptr;
+    qdec_ctx* c = new (std::nothrow) qdec_ctx();
+    if (!c) return fail(QDEC_E_OOM, "host allocation failed");
+    c->cfg = src->cfg;
+    c->sh = src->sh;
+    c->embed = src->embed;
+    c->final_norm = src->final_norm;
+    c->layers = src->layers;
+    c->stream = src->stream;
+    c->own_stream = false;
+    int rc = alloc_state(c);
+    if (rc == QDEC_OK) {
+        const Shape& sh = c->sh;
+        const size_t L = (size_t)src->position;
+        cudaError_t e = cudaSuccess;
+        if (L > 0) {
+            const size_t row = (size_t)sh.max_seq * sh.D * sizeof(bf16_t);   // one (layer, kind, head) block
+            e = cudaMemcpy2DAsync(c->kv, row, src->kv, row, L * sh.D * sizeof(bf16_t), (size_t)sh.NL * 2 * sh.HKV,
+                                  cudaMemcpyDeviceToDevice, c->stream);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(c->d_hist, src->d_hist, L * sizeof(int), cudaMemcpyDeviceToDevice, c->stream);
+        }
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(c->rope, src->rope, (size_t)sh.max_seq * (sh.D / 2) * sizeof(float2),
+                                cudaMemcpyDeviceToDevice, c->stream);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(c->d_pos, src->d_pos, sizeof(int), cudaMemcpyDeviceToDevice, c->stream);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(c->d_argmax, src->d_argmax, sizeof(int), cudaMemcpyDeviceToDevice, c->stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(c->stream);
+        if (e != cudaSuccess) rc = fail(QDEC_E_CUDA, "clone copy: %s", cudaGetErrorString(e));
+    }
+    if (rc != QDEC_OK) {
+        free_all(c);
+        delete c;
+        return rc;
+    }
+    c->position = src->position;
+    c->prefilled = src->prefilled;
+    *out = c;
+    return QDEC_OK;
+}
+
+int qdec_position(const qdec_ctx* c) {
+    if (!c) return fail(QDEC_E_INVALID_ARG, "null context");
+    return c->position;
+}
+
+int qdec_read_kv(const qdec_ctx* c, int32_t layer, int32_t kind, int32_t pos0, int32_t n_pos, void* host_dst) {
+    if (!c || !host_dst) return fail(QDEC_E_INVALID_ARG, "null argument");
+    const Shape& sh = c->sh;
+    if (layer < 0 || layer >= sh.NL || (kind != 0 && kind != 1) || pos0 < 0 || n_pos <= 0 ||
+        (int64_t)pos0 + n_pos > sh.max_seq)
+        return fail(QDEC_E_INVALID_ARG, "bad layer/kind/range");
+    qdec_ctx* m = const_cast<qdec_ctx*>(c);
+    const bf16_t* base = (kind == 0 ? m->k_cache(layer) : m->v_cache(layer)) + (size_t)pos0 * sh.D;
+    const size_t spitch = (size_t)sh.max_seq * sh.D * sizeof(bf16_t);
+    const size_t width = (size_t)n_pos * sh.D * sizeof(bf16_t);
+    CK(cudaMemcpy2DAsync(host_dst, width, base, spitch, width, sh.HKV, cudaMemcpyDeviceToHost, c->stream));
+    CK(cudaStreamSynchronize(c->stream));
+    return QDEC_OK;
+}
+
+int qdec_read_history(const qdec_ctx* c, int32_t* host_dst, int32_t n) {
+    if (!c || !host_dst || n < 0 || n > c->position) return fail(QDEC_E_INVALID_ARG, "bad history request");
+    if (n == 0) return QDEC_OK;
+    CK(cudaMemcpyAsync(host_dst, c->d_hist, (size_t)n * sizeof(int), cudaMemcpyDeviceToHost, c->stream));
+    CK(cudaStreamSynchronize(c->stream));
+    return QDEC_OK;
+}
+
+int qdec_sync(const qdec_ctx* c) {
+    if (!c) return fail(QDEC_E_INVALID_ARG, "null context");
+    CK(cudaStreamSynchronize(c->stream));
+    return QDEC_OK;
+}
+
+void qdec_destroy(qdec_ctx* c) {
+    if (!c) return;
+    if (c->stream) cudaStreamSynchronize(c->stream);
+    free_all(c);
+    delete c;
+}
+
+const char* qdec_strerror(int status) {
+    switch (status) {
+        case QDEC_OK: return "ok";
+        case QDEC_E_INVALID_ARG: return "invalid argument";
+        case QDEC_E_CAPACITY: return "KV-cache capacity exceeded";
+        case QDEC_E_STATE: return "invalid state";
+        case QDEC_E_CUDA: return "CUDA error";
+        case QDEC_E_OOM: return "out of memory";
+        case QDEC_E_TIMEOUT: return "device wait timed out";
+        case QDEC_E_UNSUPPORTED: return "unsupported model shape";
+        default: return "unknown status";
+    }
+}
+
+const char* qdec_last_error(void) { return g_last_error.c_str(); }
+
+uint64_t qdec_kernel_launches(void) { return __atomic_load_n(&qdec::g_launches, __ATOMIC_RELAXED); }
+
+}  // extern "C"

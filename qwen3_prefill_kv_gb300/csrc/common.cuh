@@ -1,0 +1,104 @@
+// Internal helpers and kernel launchers shared by the library's translation units.
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace qdec {
+
+typedef uint16_t bf16_t;   // raw bf16 bits
+
+// bf16 -> fp32 widening is exact: the bf16 bits are the high half of the fp32 word.
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ float bf1(bf16_t h) { return __uint_as_float(((uint32_t)h) << 16); }
+__device__ __forceinline__ bf16_t f2bf(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+    return (uint32_t)f2bf(lo) | ((uint32_t)f2bf(hi) << 16);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// silu(z) = z / (1 + e^-z)
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// (value, index) with "greater value wins, lower index wins a tie"; NaN never wins.
+struct ArgMax { float v; int i; };
+__device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) {
+    return v > bv || (v == bv && i < bi);
+}
+
+// Device-side model shape (mirrors qdec_config).
+struct Shape {
+    int H, NL, HQ, HKV, D, F, V, max_seq;
+    float theta, eps;
+    int qkv_rows() const { return (HQ + 2 * HKV) * D; }
+};
+
+// ---------------------------------------------------------------- launchers
+// Embedding gather + audio splice into the fp32 residual X [T, H].
+cudaError_t launch_embed_splice(const bf16_t* E, const int* ids_dev, int T, int H,
+                                const bf16_t* audio, int n_audio, int off, float* X,
+                                int* history, cudaStream_t s);
+// Decode: id = token >= 0 ? token : *prev_argmax; x = E[id]; history[*pos] = id.
+cudaError_t launch_embed_token(const bf16_t* E, int token, const int* prev_argmax,
+                               const int* pos, int H, float* x, int* history, cudaStream_t s);
+// *pos += n (keeps the device-side position of a captured decode step current).
+cudaError_t launch_advance_position(int* pos, int n, cudaStream_t s);
+// *p = v, queued on the stream (no host memory involved).
+cudaError_t launch_set_int(int* p, int v, cudaStream_t s);
+
+// Count of kernel launches issued by the library (graph replays add their kernel nodes).
+void count_launches(uint64_t n);
+// out[t] = bf16(X[t] * rsqrt(mean X[t]^2 + eps) * g)
+cudaError_t launch_rmsnorm_bf16(const float* X, int T, int H, const bf16_t* g, float eps,
+                                bf16_t* out, cudaStream_t s);
+
+enum GemmMode { GEMM_STORE_F32 = 0, GEMM_ADD_F32 = 1, GEMM_SWIGLU_BF16 = 2, GEMM_STORE_BF16 = 3 };
+// C[M, N] (op) A[M, K] . W[N, K]^T.  SWIGLU: W is [2N, K] (gate rows, then up rows at
+// offset `up_off` rows) and C_bf16[m, n] = silu(gate) * up.
+cudaError_t launch_gemm_simt(const bf16_t* A, int lda, const bf16_t* W, int M, int N, int K, int mode,
+                             int up_off, float* Cf, bf16_t* Cb, int ldc, cudaStream_t s);
+
+// Per-head RMSNorm + NeoX RoPE on q and k, V copy, KV append at slots pos0 + t.
+// qkv fp32 [T, (HQ+2HKV) D]; q_out: bf16 [T, HQ, D] (q_bf16) or fp32 (q_f32).
+cudaError_t launch_qk_norm_rope_append(const float* qkv, int T, const Shape& sh, const int* pos0,
+                                       const bf16_t* g_q, const bf16_t* g_k, const float2* rope_cs,
+                                       bf16_t* q_bf16, float* q_f32, bf16_t* k_cache, bf16_t* v_cache,
+                                       cudaStream_t s);
+
+// Prefill attention: Q bf16 [T, HQ, D] at positions pos0..pos0+T-1 over cache keys [0, pos0+T).
+cudaError_t launch_attention_prefill_simt(const bf16_t* Q, int T, const Shape& sh, int pos0,
+                                          const bf16_t* k_cache, const bf16_t* v_cache,
+                                          bf16_t* O, cudaStream_t s);
+
+// Decode attention, split over the KV length L = *pos + 1.
+// q fp32 [HQ, D]; partials sized [HQ][n_split] (+ D for o); out fp32 [HQ, D].
+int attention_decode_splits(const Shape& sh);
+cudaError_t launch_attention_decode(const float* q, const Shape& sh, const int* pos,
+                                    const bf16_t* k_cache, const bf16_t* v_cache, int n_split,
+                                    float* part_ml, float* part_o, float* out, cudaStream_t s);
+
+// Decode GEMV y = W . xhat with fp32 activations.
+enum GemvMode { GEMV_STORE = 0, GEMV_ADD = 1, GEMV_SWIGLU = 2 };
+// norm_g != nullptr: xhat = x * rsqrt(mean x^2 + eps) * norm_g, else xhat = x.
+cudaError_t launch_gemv(const bf16_t* W, int rows, int K, const float* x, const bf16_t* norm_g,
+                        float eps, int mode, int up_off, float* y, cudaStream_t s);
+
+// Tied lm_head on one row with fused final RMSNorm and a deterministic grid argmax.
+// scratch: >= lm_head_scratch_bytes(V); its first 4 bytes (ticket counter) must be zero
+// before the first launch and are returned to zero by every launch.
+size_t lm_head_scratch_bytes(int V);
+cudaError_t launch_lm_head_argmax(const bf16_t* E, int V, int H, const float* x, const bf16_t* g_final,
+                                  float eps, float* logits, int* argmax, void* scratch, cudaStream_t s);
+
+}  // namespace qdec

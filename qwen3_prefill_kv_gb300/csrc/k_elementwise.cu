@@ -1,0 +1,173 @@
+// Row-wise kernels: embedding gather + audio splice, RMSNorm, per-head Q/K RMSNorm +
+// NeoX RoPE + KV-cache append.
+//
+// "Forward map - funasr_nano", LLM decoder table: token embed (row gather), the audio-row
+// override of inputs_embeds at [fbank_beg, fbank_beg + fake_token_len), rms_norm, and the
+// per-head Q/K-RMSNorm + NeoX RoPE @ 1e6; Generation / KV Path: KV cache write.
+// "Qwen3ASR ncnn多平台移植" §5: each step builds RoPE for its absolute position and appends
+// its key/value to the cache.
+#include "common.cuh"
+
+namespace qdec {
+
+// One block per row; 8-byte loads of 4 bf16, 16-byte stores of 4 fp32.
+__global__ void embed_splice_kernel(const bf16_t* __restrict__ E, const int* __restrict__ ids, int H,
+                                    const bf16_t* __restrict__ audio, int n_audio, int off,
+                                    float* __restrict__ X, int* __restrict__ history) {
+    const int t = blockIdx.x;
+    const bool is_audio = (t >= off) && (t < off + n_audio);
+    const int id = ids[t];
+    const bf16_t* src = is_audio ? audio + (size_t)(t - off) * H : E + (size_t)id * H;
+    float* dst = X + (size_t)t * H;
+    for (int i = threadIdx.x * 4; i < H; i += blockDim.x * 4) {
+        uint2 w = *reinterpret_cast<const uint2*>(src + i);
+        *reinterpret_cast<float4*>(dst + i) = make_float4(bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
+    }
+    if (threadIdx.x == 0 && history) history[t] = id;
+}
+
+cudaError_t launch_embed_splice(const bf16_t* E, const int* ids_dev, int T, int H, const bf16_t* audio,
+                                int n_audio, int off, float* X, int* history, cudaStream_t s) {
+    embed_splice_kernel<<<T, 128, 0, s>>>(E, ids_dev, H, audio, n_audio, off, X, history);
+    return cudaGetLastError();
+}
+
+// Decode embedding: token >= 0 is embedded; -1 embeds the previous step's argmax (greedy
+// feedback kept on the device).  The token also goes into the history at slot *pos.
+__global__ void embed_token_kernel(const bf16_t* __restrict__ E, int token, const int* __restrict__ prev_argmax,
+                                   const int* __restrict__ pos, int H, float* __restrict__ x,
+                                   int* __restrict__ history) {
+    const int id = token >= 0 ? token : *prev_argmax;
+    const bf16_t* src = E + (size_t)id * H;
+    for (int i = threadIdx.x * 4; i < H; i += blockDim.x * 4) {
+        uint2 w = *reinterpret_cast<const uint2*>(src + i);
+        *reinterpret_cast<float4*>(x + i) = make_float4(bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
+    }
+    if (threadIdx.x == 0) history[*pos] = id;
+}
+
+cudaError_t launch_embed_token(const bf16_t* E, int token, const int* prev_argmax, const int* pos, int H, float* x,
+                               int* history, cudaStream_t s) {
+    embed_token_kernel<<<1, 256, 0, s>>>(E, token, prev_argmax, pos, H, x, history);
+    return cudaGetLastError();
+}
+
+__global__ void advance_position_kernel(int* pos, int n) { *pos += n; }
+__global__ void set_int_kernel(int* p, int v) { *p = v; }
+
+cudaError_t launch_set_int(int* p, int v, cudaStream_t s) {
+    set_int_kernel<<<1, 1, 0, s>>>(p, v);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_advance_position(int* pos, int n, cudaStream_t s) {
+    advance_position_kernel<<<1, 1, 0, s>>>(pos, n);
+    return cudaGetLastError();
+}
+
+// Block-wide sum over 256 threads.
+__device__ __forceinline__ float block_sum_256(float v, float* red) {
+    v = warp_sum(v);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) red[w] = v;
+    __syncthreads();
+    float r = (l < 8) ? red[l] : 0.f;
+    return warp_sum(r);
+}
+
+__global__ void rmsnorm_bf16_kernel(const float* __restrict__ X, int H, const bf16_t* __restrict__ g,
+                                    float eps, bf16_t* __restrict__ out) {
+    __shared__ float red[8];
+    const float* x = X + (size_t)blockIdx.x * H;
+    float ss = 0.f;
+    for (int i = threadIdx.x * 4; i < H; i += 1024) {
+        float4 v = *reinterpret_cast<const float4*>(x + i);
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+    ss = block_sum_256(ss, red);
+    const float r = rsqrtf(ss / (float)H + eps);
+    bf16_t* o = out + (size_t)blockIdx.x * H;
+    for (int i = threadIdx.x * 4; i < H; i += 1024) {
+        float4 v = *reinterpret_cast<const float4*>(x + i);
+        uint2 gw = *reinterpret_cast<const uint2*>(g + i);
+        uint2 ow;
+        ow.x = pack_bf2(v.x * r * bf_lo(gw.x), v.y * r * bf_hi(gw.x));
+        ow.y = pack_bf2(v.z * r * bf_lo(gw.y), v.w * r * bf_hi(gw.y));
+        *reinterpret_cast<uint2*>(o + i) = ow;
+    }
+}
+
+cudaError_t launch_rmsnorm_bf16(const float* X, int T, int H, const bf16_t* g, float eps, bf16_t* out,
+                                cudaStream_t s) {
+    rmsnorm_bf16_kernel<<<T, 256, 0, s>>>(X, H, g, eps, out);
+    return cudaGetLastError();
+}
+
+// grid (T, HQ + 2 HKV), block max(32, D/2): thread i < D/2 owns the NeoX pair (i, i + D/2) of one head.
+__global__ void qk_norm_rope_append_kernel(const float* __restrict__ qkv, int HQ, int HKV, int D, int max_seq,
+                                           float eps, const int* __restrict__ pos0,
+                                           const bf16_t* __restrict__ g_q, const bf16_t* __restrict__ g_k,
+                                           const float2* __restrict__ rope_cs,
+                                           bf16_t* __restrict__ q_bf16, float* __restrict__ q_f32,
+                                           bf16_t* __restrict__ k_cache, bf16_t* __restrict__ v_cache) {
+    __shared__ float red[4];
+    const int t = blockIdx.x, hh = blockIdx.y, i = threadIdx.x, half = D >> 1;
+    const int rows = (HQ + 2 * HKV) * D;
+    const int p = *pos0 + t;
+    const bool act = i < half;   // the block is padded to a whole warp when D/2 < 32
+    const float* src = qkv + (size_t)t * rows + (size_t)hh * D;
+    float a = act ? src[i] : 0.f, b = act ? src[i + half] : 0.f;
+    if (hh >= HQ + HKV) {  // value head: plain copy into the cache
+        const int g = hh - HQ - HKV;
+        bf16_t* dst = v_cache + ((size_t)g * max_seq + p) * D;
+        if (act) {
+            dst[i] = f2bf(a);
+            dst[i + half] = f2bf(b);
+        }
+        return;
+    }
+    float ss = warp_sum(a * a + b * b);
+    if (half > 32) {
+        if ((i & 31) == 0) red[i >> 5] = ss;
+        __syncthreads();
+        ss = 0.f;
+        for (int w = 0; w < (half >> 5); ++w) ss += red[w];
+    }
+    const float r = rsqrtf(ss / (float)D + eps);
+    if (!act) return;
+    const bf16_t* g = hh < HQ ? g_q : g_k;
+    a *= r * bf1(g[i]);
+    b *= r * bf1(g[i + half]);
+    const float2 cs = rope_cs[(size_t)p * half + i];
+    const float ra = a * cs.x - b * cs.y;
+    const float rb = b * cs.x + a * cs.y;
+    if (hh < HQ) {
+        if (q_bf16) {
+            bf16_t* dst = q_bf16 + ((size_t)t * HQ + hh) * D;
+            dst[i] = f2bf(ra);
+            dst[i + half] = f2bf(rb);
+        } else {
+            float* dst = q_f32 + ((size_t)t * HQ + hh) * D;
+            dst[i] = ra;
+            dst[i + half] = rb;
+        }
+    } else {
+        const int g2 = hh - HQ;
+        bf16_t* dst = k_cache + ((size_t)g2 * max_seq + p) * D;
+        dst[i] = f2bf(ra);
+        dst[i + half] = f2bf(rb);
+    }
+}
+
+cudaError_t launch_qk_norm_rope_append(const float* qkv, int T, const Shape& sh, const int* pos0,
+                                       const bf16_t* g_q, const bf16_t* g_k, const float2* rope_cs,
+                                       bf16_t* q_bf16, float* q_f32, bf16_t* k_cache, bf16_t* v_cache,
+                                       cudaStream_t s) {
+    dim3 grid(T, sh.HQ + 2 * sh.HKV);
+    qk_norm_rope_append_kernel<<<grid, sh.D / 2 < 32 ? 32 : sh.D / 2, 0, s>>>(qkv, sh.HQ, sh.HKV, sh.D, sh.max_seq, sh.eps, pos0,
+                                                         g_q, g_k, rope_cs, q_bf16, q_f32, k_cache, v_cache);
+    return cudaGetLastError();
+}
+
+}  // namespace qdec

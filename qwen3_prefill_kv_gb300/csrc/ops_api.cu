@@ -1,0 +1,60 @@
+// Per-kernel C entry points (include/qdec_ops.h).
+#include "../../include/qdec.h"
+#include "../../include/qdec_ops.h"
+#include "common.cuh"
+
+using namespace qdec;
+
+namespace {
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? QDEC_OK : QDEC_E_CUDA; }
+}
+
+extern "C" {
+
+int qdec_op_gemm(const void* A, int32_t lda, const void* W, int32_t M, int32_t N, int32_t K, int32_t mode,
+                 int32_t up_off, void* C, int32_t ldc, int32_t impl, void* stream) {
+    if (!A || !W || !C || M <= 0 || N <= 0 || K <= 0 || mode < 0 || mode > 3) return QDEC_E_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool f32 = (mode == QDEC_GEMM_STORE_F32 || mode == QDEC_GEMM_ADD_F32);
+    float* Cf = f32 ? static_cast<float*>(C) : nullptr;
+    bf16_t* Cb = f32 ? nullptr : static_cast<bf16_t*>(C);
+    if (impl == QDEC_IMPL_SIMT) {
+        if (K % 32 != 0 || lda % 8 != 0) return QDEC_E_UNSUPPORTED;
+        return cuda_status(launch_gemm_simt(static_cast<const bf16_t*>(A), lda, static_cast<const bf16_t*>(W), M, N,
+                                            K, mode, up_off, Cf, Cb, ldc, s));
+    }
+    return QDEC_E_UNSUPPORTED;
+}
+
+int qdec_op_attention_prefill(const void* Q, int32_t T, int32_t HQ, int32_t HKV, int32_t D, int32_t max_seq,
+                              int32_t pos0, const void* k_cache, const void* v_cache, void* O, int32_t impl,
+                              void* stream) {
+    if (!Q || !k_cache || !v_cache || !O || T <= 0 || HQ <= 0 || HKV <= 0 || HQ % HKV != 0 || pos0 < 0 ||
+        pos0 + T > max_seq)
+        return QDEC_E_INVALID_ARG;
+    Shape sh{};
+    sh.HQ = HQ;
+    sh.HKV = HKV;
+    sh.D = D;
+    sh.max_seq = max_seq;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (impl == QDEC_IMPL_SIMT)
+        return cuda_status(launch_attention_prefill_simt(static_cast<const bf16_t*>(Q), T, sh, pos0,
+                                                         static_cast<const bf16_t*>(k_cache),
+                                                         static_cast<const bf16_t*>(v_cache), static_cast<bf16_t*>(O), s));
+    return QDEC_E_UNSUPPORTED;
+}
+
+size_t qdec_op_lm_head_scratch_bytes(int32_t V) { return V > 0 ? lm_head_scratch_bytes(V) : 0; }
+
+int qdec_op_lm_head_argmax(const void* E, int32_t V, int32_t H, const float* x, const void* g_final, float eps,
+                           float* logits, int32_t* argmax, void* scratch, size_t scratch_bytes, void* stream) {
+    if (!E || !x || !g_final || !logits || !argmax || !scratch || V <= 0 || H <= 0 || H % 8 != 0)
+        return QDEC_E_INVALID_ARG;
+    if (scratch_bytes < lm_head_scratch_bytes(V)) return QDEC_E_INVALID_ARG;
+    return cuda_status(launch_lm_head_argmax(static_cast<const bf16_t*>(E), V, H, x,
+                                             static_cast<const bf16_t*>(g_final), eps, logits, argmax, scratch,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+"""Full-size parity (Qwen3-0.6B shape: hidden 1024, 28 layers, GQA 16/8, head_dim
+128, ffn 3072, vocab 151936) on the workloads' own prompt layouts, teacher-forced
+against the float64 oracle ("Qwen3ASR ncnn多平台移植" §7.1-§7.2)."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from qwen3_prefill_kv_gb300 import synth
+from qwen3_prefill_kv_gb300._lib import Decoder
+
+import _harness as H
+
+pytestmark = pytest.mark.gpu
+SH = synth.QWEN3_06B
+
+
+@pytest.fixture(scope="module")
+def full():
+    w = synth.make_weights(SH, seed=0)
+    return w, w.to("cuda"), H.make_oracle(w)
+
+
+def _report(name, res):
+    out = os.environ.get("QDEC_PARITY_REPORT_DIR")
+    ms = [oracle.step_metrics(g, r) for g, r, _ in res]
+    summary = {"workload": name, "steps": len(ms),
+               "min_cosine": min(m["cosine"] for m in ms),
+               "max_abs_over_max_ref": max(m["max_abs"] / m["max_abs_ref"] for m in ms),
+               "mean_abs": float(np.mean([m["mean_abs"] for m in ms])),
+               "rmse": float(np.mean([m["rmse"] for m in ms])),
+               "max_mean_rel": max(m["mean_rel"] for m in ms),
+               "argmax_agreement": float(np.mean([m["argmax_equal"] for m in ms]))}
+    print(json.dumps(summary))
+    if out:
+        os.makedirs(out, exist_ok=True)
+        with open(os.path.join(out, f"parity_{name}.json"), "w") as f:
+            json.dump({"summary": summary, "per_step": ms}, f, indent=1)
+    return summary
+
+
+@pytest.mark.parametrize("name", ["funasr_nano_short", "qwen3_asr_30s"])
+def test_teacher_forced_workload(full, name):
+    w, wd, orc = full
+    wl = synth.WORKLOADS[name]
+    p = synth.make_prompt(wl, seed=0)
+    dec = Decoder(SH, wd, max_seq=wl.max_seq)
+    res = H.teacher_forced(dec, orc.clone(), p, wl.n_decode)
+    H.assert_step_parity(res, name)
+    _report(name, res)
+    hist = dec.read_history()
+    assert hist.size == wl.max_seq
+    kv_prompt = p.ids.numpy().copy()
+    mask = np.ones(kv_prompt.size, bool); mask[wl.audio_offset:wl.audio_offset + wl.n_audio] = False
+    assert np.array_equal(hist[:wl.n_prompt][mask], kv_prompt[mask])
+
+
+@pytest.mark.slow
+def test_long_context_prefill_and_steps(full):
+    w, wd, orc = full
+    wl = synth.WORKLOADS["long_context"]
+    p = synth.make_prompt(wl, seed=0)
+    dec = Decoder(SH, wd, max_seq=wl.max_seq)
+    res = H.teacher_forced(dec, orc.clone(), p, 2)
+    H.assert_step_parity(res, "long_context")
+    _report("long_context", res)
+
+
+def test_branching_batch(full):
+    w, wd, orc = full
+    wl = synth.WORKLOADS["branching_b64"]
+    p = synth.make_prompt(wl, seed=0)
+    src = Decoder(SH, wd, max_seq=wl.max_seq)
+    src.prefill(p.ids, p.audio.cuda(), p.audio_offset)
+    o_src = orc.clone(); o_src.prefill(p.ids.numpy(), H.audio_f64(p), p.audio_offset)
+    n = wl.batch
+    branches = [src.clone() for _ in range(n)]
+    toks = synth.make_tokens(SH.vocab, n, seed=0).numpy()
+    sample = [0, 31, 63]
+    obr = {i: o_src.clone() for i in sample}
+    lb = torch.empty(n, SH.vocab, device="cuda")
+    for step in range(3):
+        am = Decoder.decode_step_batch(branches, toks, logits=lb)
+        got = lb.cpu().numpy()
+        assert np.array_equal(am, got.argmax(axis=1))
+        for i in sample:
+            z = obr[i].decode_step(int(toks[i]))
+            ok, m = oracle.parity_gate(got[i], z, H.COS_MIN, H.REL_BOUND)
+            assert ok, (step, i, m)
+        toks = am
+    assert all(b.position == wl.n_prompt + 3 for b in branches)

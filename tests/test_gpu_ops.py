@@ -1,0 +1,104 @@
+"""Single-kernel parity through the per-kernel C entry points: GEMM epilogues,
+prefill attention and the lm_head + argmax, each against float64 on the same
+bf16 inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from qwen3_prefill_kv_gb300 import _lib
+
+pytestmark = pytest.mark.gpu
+
+
+def _bf16(shape, seed, std=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(*shape, generator=g) * std).to(torch.bfloat16)
+
+
+def _gemm_ref(A, W, mode, N, up_off):
+    a = A.double(); w = W.double()
+    if mode == _lib.GEMM_SWIGLU_BF16:
+        return torch.from_numpy(oracle.swiglu(torch.cat([a @ w[:N].T, a @ w[up_off:up_off + N].T], 1).numpy(), N))
+    return a @ w[:N].T
+
+
+GEMM_CASES = [(1, 256, 128), (37, 256, 128), (130, 384, 384), (77, 4096, 1024), (64, 1024, 2048),
+              (415, 1024, 3072)]
+
+
+@pytest.mark.parametrize("impl", [_lib.IMPL_SIMT])
+@pytest.mark.parametrize("M,N,K", GEMM_CASES)
+@pytest.mark.parametrize("mode", [_lib.GEMM_STORE_F32, _lib.GEMM_ADD_F32, _lib.GEMM_SWIGLU_BF16, _lib.GEMM_STORE_BF16])
+def test_gemm_epilogues(impl, M, N, K, mode):
+    A = _bf16((M, K), 1)
+    rows = 2 * N if mode == _lib.GEMM_SWIGLU_BF16 else N
+    W = _bf16((rows, K), 2, std=0.02)
+    ref = _gemm_ref(A, W, mode, N, N)
+    if mode in (_lib.GEMM_STORE_F32, _lib.GEMM_ADD_F32):
+        C0 = torch.randn(M, N) if mode == _lib.GEMM_ADD_F32 else torch.zeros(M, N)
+        Cd = C0.cuda()
+        _lib.gemm(A.cuda(), W.cuda(), M, N, K, mode, Cd, up_off=N, impl=impl)
+        got = Cd.cpu().double() - (C0.double() if mode == _lib.GEMM_ADD_F32 else 0)
+        tol = 2e-5 * ref.abs().max().item() + 1e-6
+    else:
+        Cd = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
+        _lib.gemm(A.cuda(), W.cuda(), M, N, K, mode, Cd, up_off=N, impl=impl)
+        got = Cd.cpu().double()
+        tol = 8e-3 * ref.abs().max().item()
+    torch.cuda.synchronize()
+    assert (got - ref).abs().max().item() <= tol
+
+
+ATTN_CASES = [(77, 4, 2, 32, 0), (64, 16, 8, 128, 0), (200, 16, 8, 128, 0), (33, 4, 2, 32, 40), (5, 16, 8, 128, 100)]
+
+
+@pytest.mark.parametrize("impl", [_lib.IMPL_SIMT])
+@pytest.mark.parametrize("T,HQ,HKV,D,pos0", ATTN_CASES)
+def test_attention_prefill(impl, T, HQ, HKV, D, pos0):
+    L = pos0 + T
+    max_seq = L + 7
+    Q = _bf16((T, HQ, D), 3)
+    K = _bf16((HKV, max_seq, D), 4)
+    Vv = _bf16((HKV, max_seq, D), 5)
+    O = torch.zeros(T, HQ * D, dtype=torch.bfloat16, device="cuda")
+    _lib.attention_prefill(Q.cuda(), T, HQ, HKV, D, max_seq, pos0, K.cuda(), Vv.cuda(), O, impl=impl)
+    torch.cuda.synchronize()
+    ref = oracle.causal_gqa_attention(Q.double().numpy(), K[:, :L].permute(1, 0, 2).double().numpy(),
+                                      Vv[:, :L].permute(1, 0, 2).double().numpy(),
+                                      np.arange(pos0, pos0 + T), np.arange(L)).reshape(T, HQ * D)
+    got = O.cpu().double().numpy()
+    assert np.abs(got - ref).max() <= 1e-2 * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("V,H", [(1024, 128), (151936, 1024), (1000, 256)])
+def test_lm_head_argmax(V, H):
+    E = _bf16((V, H), 6, std=0.02)
+    x = torch.randn(H, generator=torch.Generator().manual_seed(7)) * 3
+    g = (1 + 0.1 * torch.randn(H, generator=torch.Generator().manual_seed(8))).to(torch.bfloat16)
+    scratch = torch.zeros(_lib.lm_head_scratch_bytes(V), dtype=torch.uint8, device="cuda")
+    logits = torch.empty(V, device="cuda")
+    am = torch.empty(1, dtype=torch.int32, device="cuda")
+    for _ in range(2):      # the second call checks that the ticket counter was returned to zero
+        _lib.lm_head_argmax(E.cuda(), V, H, x.cuda(), g.cuda(), 1e-6, logits, am, scratch)
+        torch.cuda.synchronize()
+        h = oracle.rms_norm(x.double().numpy(), g.double().numpy(), 1e-6)
+        ref = oracle.tied_lm_head(E.double().numpy(), h)
+        got = logits.cpu().double().numpy()
+        assert np.abs(got - ref).max() <= 1e-4 * np.abs(ref).max()
+        assert int(am.item()) == int(np.argmax(got))
+
+
+def test_lm_head_tie_takes_lowest_index():
+    V, H = 4096, 128
+    E = _bf16((V, H), 9, std=0.02)
+    x = torch.randn(H, generator=torch.Generator().manual_seed(10))
+    best = int(torch.argmax(E.float() @ x))
+    E[3000] = E[best]; E[17] = E[best]; E[best] = E[best]      # three identical maximal rows
+    g = torch.ones(H, dtype=torch.bfloat16)
+    scratch = torch.zeros(_lib.lm_head_scratch_bytes(V), dtype=torch.uint8, device="cuda")
+    logits = torch.empty(V, device="cuda")
+    am = torch.empty(1, dtype=torch.int32, device="cuda")
+    _lib.lm_head_argmax(E.cuda(), V, H, x.cuda(), g.cuda(), 1e-6, logits, am, scratch)
+    torch.cuda.synchronize()
+    assert int(am.item()) == min(17, best)

@@ -1,0 +1,215 @@
+"""GPU parity on the tiny Qwen3-style decoder (hidden 128, 2 layers, 4/2 heads,
+head_dim 32, ffn 384, vocab 1024): every call goes through the C ABI and is
+compared with the float64 oracle on the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from qwen3_prefill_kv_gb300 import synth
+from qwen3_prefill_kv_gb300._lib import Decoder, QdecError
+
+import _harness as H
+
+pytestmark = pytest.mark.gpu
+SH = synth.TINY
+
+
+@pytest.fixture(scope="module")
+def model():
+    w = synth.make_weights(SH, seed=0)
+    return w, w.to("cuda"), H.make_oracle(w)
+
+
+@pytest.fixture(scope="module")
+def model_jitter():
+    w = synth.make_weights(SH, seed=5, gain_jitter=True)
+    return w, w.to("cuda"), H.make_oracle(w)
+
+
+def _prompt(n_prefix, n_audio, n_suffix, seed=0):
+    wl = synth.Workload("t", SH, n_prefix, n_audio, n_suffix, 0)
+    return synth.make_prompt(wl, seed)
+
+
+LAYOUTS = [(12, 8, 12, 16),     # the tiny workload: 32 positions, 16 steps
+           (12, 50, 15, 8),     # 77 positions: two 64-row tiles + ragged tail
+           (0, 20, 5, 4),       # audio at offset 0
+           (10, 6, 0, 4),       # audio ends at the last position
+           (40, 0, 0, 4),       # text only
+           (1, 0, 0, 3),        # a single-token prompt
+           (3, 130, 2, 2)]      # 135 positions
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+def test_teacher_forced_logits(model, layout):
+    w, wd, orc = model
+    n_prefix, n_audio, n_suffix, steps = layout
+    p = _prompt(n_prefix, n_audio, n_suffix)
+    dec = Decoder(SH, wd, max_seq=p.ids.numel() + steps)
+    res = H.teacher_forced(dec, orc, p, steps)
+    H.assert_step_parity(res, f"tiny {layout}")
+    assert dec.position == p.ids.numel() + steps
+
+
+def test_gain_jitter(model_jitter):
+    w, wd, orc = model_jitter
+    p = _prompt(12, 8, 12)
+    dec = Decoder(SH, wd, max_seq=48)
+    H.assert_step_parity(H.teacher_forced(dec, orc, p, 8), "tiny gains")
+
+
+def test_kv_slots_match_oracle_positions(model):
+    w, wd, orc = model
+    p = _prompt(12, 8, 12)
+    steps = 5
+    dec = Decoder(SH, wd, max_seq=64)
+    H.teacher_forced(dec, orc, p, steps)
+    L = p.ids.numel() + steps
+    for l in range(SH.n_layers):
+        for kind, ref in ((0, orc.k_cache[l]), (1, orc.v_cache[l])):
+            got = dec.read_kv(l, kind, 0, 64)                       # [HKV, 64, D] bf16 bits
+            g = (got.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            assert not g[:, L:].any(), "slots beyond the written positions must stay untouched"
+            r = np.transpose(ref, (1, 0, 2))                        # [HKV, L, D]
+            gl = g[:, :L]
+            assert np.abs(gl - r).max() <= 2e-2 * np.abs(r).max()
+            # slot index == absolute position: each slot is nearest to its own position
+            for h in range(SH.n_kv_heads):
+                d = ((gl[h][:, None, :] - r[h][None, :, :]) ** 2).sum(-1)
+                assert np.array_equal(d.argmin(axis=1), np.arange(L))
+
+
+def test_history_and_device_feedback(model):
+    w, wd, orc = model
+    p = _prompt(12, 8, 12)
+    a = Decoder(SH, wd, max_seq=48)
+    b = Decoder(SH, wd, max_seq=48)
+    la = torch.empty(SH.vocab, device="cuda")
+    lb = torch.empty(SH.vocab, device="cuda")
+    ta = a.prefill(p.ids, p.audio.cuda(), p.audio_offset)
+    tb = b.prefill(p.ids, p.audio.cuda(), p.audio_offset)
+    assert ta == tb
+    for _ in range(10):
+        a.decode_step(-1, want_argmax=False)          # greedy feedback stays on the device
+        tb = b.decode_step(tb, logits=lb)             # host round trip
+    a.decode_step(-1, logits=la, want_argmax=False)
+    b.decode_step(tb, logits=lb)
+    ha, hb = a.read_history(), b.read_history()
+    assert np.array_equal(ha, hb)
+    assert np.array_equal(ha[:12], p.ids.numpy()[:12])
+    assert torch.equal(la, lb)
+
+
+def test_repeat_runs_are_bitwise_identical(model):
+    w, wd, orc = model
+    p = _prompt(12, 50, 15)
+    outs = []
+    for _ in range(2):
+        dec = Decoder(SH, wd, max_seq=80)
+        lg = torch.empty(SH.vocab, device="cuda")
+        dec.prefill(p.ids, p.audio.cuda(), p.audio_offset, logits=lg)
+        seq = [lg.clone()]
+        for t in (3, 4, 5):
+            dec.decode_step(t, logits=lg)
+            seq.append(lg.clone())
+        outs.append(torch.stack(seq))
+    assert torch.equal(outs[0], outs[1])
+
+
+def test_host_and_device_buffers_agree(model):
+    w, wd, orc = model
+    p = _prompt(12, 8, 12)
+    d1 = Decoder(SH, wd, max_seq=40)
+    d2 = Decoder(SH, wd, max_seq=40)
+    l1 = torch.empty(SH.vocab, device="cuda")
+    l2 = torch.empty(SH.vocab).pin_memory()
+    l3 = torch.empty(SH.vocab)                      # pageable host memory
+    a1 = d1.prefill(p.ids, p.audio.cuda(), p.audio_offset, logits=l1)
+    a2 = d2.prefill(p.ids, p.audio, p.audio_offset, logits=l2)     # host audio rows
+    assert a1 == a2 and torch.equal(l1.cpu(), l2)
+    d1.decode_step(7, logits=l1)
+    d2.decode_step(7, logits=l3)
+    assert torch.equal(l1.cpu(), l3)
+
+
+def test_clone_branches(model):
+    w, wd, orc = model
+    p = _prompt(12, 8, 12)
+    src = Decoder(SH, wd, max_seq=48)
+    src.prefill(p.ids, p.audio.cuda(), p.audio_offset)
+    o_src = orc.clone(); o_src.prefill(p.ids.numpy(), H.audio_f64(p), p.audio_offset)
+    c1 = src.clone()
+    assert c1.position == src.position
+    lg_a = torch.empty(SH.vocab, device="cuda"); lg_b = torch.empty(SH.vocab, device="cuda")
+    # identical inputs: clone and source stay bitwise equal
+    src.decode_step(11, logits=lg_a); c1.decode_step(11, logits=lg_b)
+    assert torch.equal(lg_a, lg_b)
+    # divergent branches each match an oracle branch
+    o_a = o_src.clone(); o_b = o_src.clone()
+    za = o_a.decode_step(11); zb = o_b.decode_step(11)
+    for ta, tb in ((20, 900), (21, 901), (22, 902)):
+        src.decode_step(ta, logits=lg_a); c1.decode_step(tb, logits=lg_b)
+        za = o_a.decode_step(ta); zb = o_b.decode_step(tb)
+        for g, r in ((lg_a, za), (lg_b, zb)):
+            ok, m = oracle.parity_gate(g.cpu().numpy(), r, H.COS_MIN, H.REL_BOUND)
+            assert ok, m
+    assert src.read_history()[-3:].tolist() == [20, 21, 22]
+    assert c1.read_history()[-3:].tolist() == [900, 901, 902]
+
+
+def test_batch_step_matches_single_streams(model):
+    w, wd, orc = model
+    p = _prompt(12, 8, 12)
+    src = Decoder(SH, wd, max_seq=48)
+    src.prefill(p.ids, p.audio.cuda(), p.audio_offset)
+    o_src = orc.clone(); o_src.prefill(p.ids.numpy(), H.audio_f64(p), p.audio_offset)
+    n = 5
+    branches = [src.clone() for _ in range(n)]
+    singles = [src.clone() for _ in range(n)]
+    obr = [o_src.clone() for _ in range(n)]
+    toks = synth.make_tokens(SH.vocab, n, seed=3).numpy()
+    lb = torch.empty(n, SH.vocab, device="cuda")
+    ls = torch.empty(SH.vocab, device="cuda")
+    for step in range(4):
+        am = Decoder.decode_step_batch(branches, toks, logits=lb)
+        for i in range(n):
+            a1 = singles[i].decode_step(int(toks[i]), logits=ls)
+            z = obr[i].decode_step(int(toks[i]))
+            ok, m = oracle.parity_gate(lb[i].cpu().numpy(), z, H.COS_MIN, H.REL_BOUND)
+            assert ok, (step, i, m)
+            assert am[i] == int(torch.argmax(lb[i]))
+            np.testing.assert_allclose(lb[i].cpu().numpy(), ls.cpu().numpy(), rtol=0,
+                                       atol=1e-3 * float(ls.abs().max()))
+        toks = am                                    # greedy continuation per stream
+    assert all(b.position == p.ids.numel() + 4 for b in branches)
+
+
+def test_errors_leave_context_unchanged(model):
+    w, wd, orc = model
+    p = _prompt(12, 8, 12)
+    dec = Decoder(SH, wd, max_seq=33)
+    with pytest.raises(QdecError) as e:
+        dec.decode_step(1)
+    assert e.value.status == -3                      # decode before prefill
+    bad = p.ids.clone(); bad[3] = SH.vocab
+    with pytest.raises(QdecError) as e:
+        dec.prefill(bad, p.audio.cuda(), p.audio_offset)
+    assert e.value.status == -1
+    with pytest.raises(QdecError) as e:
+        dec.prefill(p.ids, p.audio.cuda(), 30)       # audio rows past the prompt end
+    assert e.value.status == -1
+    long_ids = torch.zeros(34, dtype=torch.int32)
+    with pytest.raises(QdecError) as e:
+        dec.prefill(long_ids)
+    assert e.value.status == -2
+    dec.prefill(p.ids, p.audio.cuda(), p.audio_offset)
+    assert dec.position == 32
+    dec.decode_step(5)
+    with pytest.raises(QdecError) as e:
+        dec.decode_step(6)                           # slot 33 >= max_seq
+    assert e.value.status == -2
+    with pytest.raises(QdecError) as e:
+        dec.decode_step(-2)
+    assert e.value.status == -1
+    assert dec.position == 33
