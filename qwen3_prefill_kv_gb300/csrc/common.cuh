@@ -59,6 +59,8 @@ cudaError_t launch_set_int(int* p, int v, cudaStream_t s);
 
 // Count of kernel launches issued by the library (graph replays add their kernel nodes).
 void count_launches(uint64_t n);
+// Records a message for qdec_last_error() and returns `code`.
+int set_error(int code, const char* fmt, ...);
 // out[t] = bf16(X[t] * rsqrt(mean X[t]^2 + eps) * g)
 cudaError_t launch_rmsnorm_bf16(const float* X, int T, int H, const bf16_t* g, float eps,
                                 bf16_t* out, cudaStream_t s);

@@ -204,6 +204,7 @@ __global__ void attn_decode_merge_kernel(int D, int n_split, const float* __rest
 template <int D>
 cudaError_t launch_decode_d(const float* q, const Shape& sh, const int* pos, const bf16_t* kc, const bf16_t* vc,
                             int n_split, float* part_ml, float* part_o, cudaStream_t s) {
+    (void)cudaGetLastError();   // attribute only this launch's errors
     dim3 grid(sh.HKV, n_split);
     switch (sh.HQ / sh.HKV) {
         case 1: attn_decode_kernel<D, 1><<<grid, DNT, 0, s>>>(q, sh.max_seq, pos, kc, vc, n_split, part_ml, part_o); break;
@@ -219,6 +220,7 @@ cudaError_t launch_decode_d(const float* q, const Shape& sh, const int* pos, con
 
 cudaError_t launch_attention_prefill_simt(const bf16_t* Q, int T, const Shape& sh, int pos0, const bf16_t* k_cache,
                                           const bf16_t* v_cache, bf16_t* O, cudaStream_t s) {
+    (void)cudaGetLastError();   // attribute only this launch's errors
     dim3 grid((T + PBQ - 1) / PBQ, sh.HQ);
     switch (sh.D) {
         case 32: attn_prefill_simt_kernel<32><<<grid, PNT, 0, s>>>(Q, T, sh.HQ, sh.HKV, sh.max_seq, pos0, k_cache, v_cache, O); break;
@@ -237,6 +239,7 @@ int attention_decode_splits(const Shape& sh) {
 cudaError_t launch_attention_decode(const float* q, const Shape& sh, const int* pos, const bf16_t* k_cache,
                                     const bf16_t* v_cache, int n_split, float* part_ml, float* part_o, float* out,
                                     cudaStream_t s) {
+    (void)cudaGetLastError();   // attribute only this launch's errors
     cudaError_t e;
     switch (sh.D) {
         case 32: e = launch_decode_d<32>(q, sh, pos, k_cache, v_cache, n_split, part_ml, part_o, s); break;

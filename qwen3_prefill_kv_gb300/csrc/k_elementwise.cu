@@ -28,6 +28,7 @@ __global__ void embed_splice_kernel(const bf16_t* __restrict__ E, const int* __r
 
 cudaError_t launch_embed_splice(const bf16_t* E, const int* ids_dev, int T, int H, const bf16_t* audio,
                                 int n_audio, int off, float* X, int* history, cudaStream_t s) {
+    (void)cudaGetLastError();   // attribute only this launch's errors
     embed_splice_kernel<<<T, 128, 0, s>>>(E, ids_dev, H, audio, n_audio, off, X, history);
     return cudaGetLastError();
 }
@@ -48,6 +49,7 @@ __global__ void embed_token_kernel(const bf16_t* __restrict__ E, int token, cons
 
 cudaError_t launch_embed_token(const bf16_t* E, int token, const int* prev_argmax, const int* pos, int H, float* x,
                                int* history, cudaStream_t s) {
+    (void)cudaGetLastError();   // attribute only this launch's errors
     embed_token_kernel<<<1, 256, 0, s>>>(E, token, prev_argmax, pos, H, x, history);
     return cudaGetLastError();
 }
@@ -56,11 +58,13 @@ __global__ void advance_position_kernel(int* pos, int n) { *pos += n; }
 __global__ void set_int_kernel(int* p, int v) { *p = v; }
 
 cudaError_t launch_set_int(int* p, int v, cudaStream_t s) {
+    (void)cudaGetLastError();   // attribute only this launch's errors
     set_int_kernel<<<1, 1, 0, s>>>(p, v);
     return cudaGetLastError();
 }
 
 cudaError_t launch_advance_position(int* pos, int n, cudaStream_t s) {
+    (void)cudaGetLastError();   // attribute only this launch's errors
     advance_position_kernel<<<1, 1, 0, s>>>(pos, n);
     return cudaGetLastError();
 }
@@ -100,6 +104,7 @@ __global__ void rmsnorm_bf16_kernel(const float* __restrict__ X, int H, const bf
 
 cudaError_t launch_rmsnorm_bf16(const float* X, int T, int H, const bf16_t* g, float eps, bf16_t* out,
                                 cudaStream_t s) {
+    (void)cudaGetLastError();   // attribute only this launch's errors
     rmsnorm_bf16_kernel<<<T, 256, 0, s>>>(X, H, g, eps, out);
     return cudaGetLastError();
 }
@@ -164,6 +169,7 @@ cudaError_t launch_qk_norm_rope_append(const float* qkv, int T, const Shape& sh,
                                        const bf16_t* g_q, const bf16_t* g_k, const float2* rope_cs,
                                        bf16_t* q_bf16, float* q_f32, bf16_t* k_cache, bf16_t* v_cache,
                                        cudaStream_t s) {
+    (void)cudaGetLastError();   // attribute only this launch's errors
     dim3 grid(T, sh.HQ + 2 * sh.HKV);
     qk_norm_rope_append_kernel<<<grid, sh.D / 2 < 32 ? 32 : sh.D / 2, 0, s>>>(qkv, sh.HQ, sh.HKV, sh.D, sh.max_seq, sh.eps, pos0,
                                                          g_q, g_k, rope_cs, q_bf16, q_f32, k_cache, v_cache);

@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(const bf16_t* __restrict_
 
 cudaError_t launch_gemm_simt(const bf16_t* A, int lda, const bf16_t* W, int M, int N, int K, int mode, int up_off,
                              float* Cf, bf16_t* Cb, int ldc, cudaStream_t s) {
+    (void)cudaGetLastError();   // attribute only this launch's errors
     if (K % BK != 0 || lda % 8 != 0) return cudaErrorInvalidValue;
     dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
     switch (mode) {

@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(GEMV_THREADS) lm_head_argmax_kernel(const bf16
 
 cudaError_t launch_gemv(const bf16_t* W, int rows, int K, const float* x, const bf16_t* norm_g, float eps,
                         int mode, int up_off, float* y, cudaStream_t s) {
+    (void)cudaGetLastError();   // attribute only this launch's errors
     if (K % 8 != 0) return cudaErrorInvalidValue;
     constexpr int R = 2;
     const int grid = (rows + (GEMV_THREADS / 32) * R - 1) / ((GEMV_THREADS / 32) * R);
@@ -200,6 +201,7 @@ size_t lm_head_scratch_bytes(int V) {
 
 cudaError_t launch_lm_head_argmax(const bf16_t* E, int V, int H, const float* x, const bf16_t* g_final, float eps,
                                   float* logits, int* argmax, void* scratch, cudaStream_t s) {
+    (void)cudaGetLastError();   // attribute only this launch's errors
     if (H % 8 != 0) return cudaErrorInvalidValue;
     const int grid = (V + LM_ROWS_PER_BLOCK - 1) / LM_ROWS_PER_BLOCK;
     lm_head_argmax_kernel<<<grid, GEMV_THREADS, (size_t)H * sizeof(float), s>>>(E, V, H, x, g_final, eps, logits,

@@ -6,20 +6,24 @@
 using namespace qdec;
 
 namespace {
-int cuda_status(cudaError_t e) { return e == cudaSuccess ? QDEC_OK : QDEC_E_CUDA; }
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return QDEC_OK;
+    return set_error(QDEC_E_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+}
 }
 
 extern "C" {
 
 int qdec_op_gemm(const void* A, int32_t lda, const void* W, int32_t M, int32_t N, int32_t K, int32_t mode,
                  int32_t up_off, void* C, int32_t ldc, int32_t impl, void* stream) {
-    if (!A || !W || !C || M <= 0 || N <= 0 || K <= 0 || mode < 0 || mode > 3) return QDEC_E_INVALID_ARG;
+    if (!A || !W || !C || M <= 0 || N <= 0 || K <= 0 || mode < 0 || mode > 3)
+        return set_error(QDEC_E_INVALID_ARG, "qdec_op_gemm: null pointer or bad size/mode");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool f32 = (mode == QDEC_GEMM_STORE_F32 || mode == QDEC_GEMM_ADD_F32);
     float* Cf = f32 ? static_cast<float*>(C) : nullptr;
     bf16_t* Cb = f32 ? nullptr : static_cast<bf16_t*>(C);
     if (impl == QDEC_IMPL_SIMT) {
-        if (K % 32 != 0 || lda % 8 != 0) return QDEC_E_UNSUPPORTED;
+        if (K % 32 != 0 || lda % 8 != 0) return set_error(QDEC_E_UNSUPPORTED, "SIMT GEMM needs K %% 32 == 0, lda %% 8 == 0");
         return cuda_status(launch_gemm_simt(static_cast<const bf16_t*>(A), lda, static_cast<const bf16_t*>(W), M, N,
                                             K, mode, up_off, Cf, Cb, ldc, s));
     }

@@ -74,10 +74,14 @@ def test_kv_slots_match_oracle_positions(model):
             r = np.transpose(ref, (1, 0, 2))                        # [HKV, L, D]
             gl = g[:, :L]
             assert np.abs(gl - r).max() <= 2e-2 * np.abs(r).max()
-            # slot index == absolute position: each slot is nearest to its own position
+            # slot index == absolute position: each slot's own position attains the minimum
+            # distance (V rows of repeated tokens can coincide, so ties are allowed)
             for h in range(SH.n_kv_heads):
                 d = ((gl[h][:, None, :] - r[h][None, :, :]) ** 2).sum(-1)
-                assert np.array_equal(d.argmin(axis=1), np.arange(L))
+                own = d[np.arange(L), np.arange(L)]
+                assert np.all(own <= d.min(axis=1) + 1e-12)
+                if kind == 0:   # RoPE makes every position's key distinct: strict
+                    assert np.array_equal(d.argmin(axis=1), np.arange(L))
 
 
 def test_history_and_device_feedback(model):
