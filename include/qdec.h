@@ -81,7 +81,10 @@ typedef struct qdec_ctx qdec_ctx;
  * allocates the KV cache [n_layers][2][n_kv_heads][max_seq][head_dim] bf16,
  * the decode scratch and a RoPE cos/sin table [max_seq][head_dim/2] (angles
  * p * theta^(-2i/D) evaluated in double on the host, stored as fp32).
- * `cuda_stream` is a cudaStream_t or NULL.  *out receives the context. */
+ * `cuda_stream` is a cudaStream_t that must outlive this context and its
+ * clones, or NULL: the library then creates a stream, shares it with the
+ * context's clones and destroys it with the last of them.  *out receives the
+ * context. */
 int qdec_create(const qdec_config *cfg, const qdec_weights *w, void *cuda_stream, qdec_ctx **out);
 
 /* Prefill ("Forward map - funasr_nano", Generation / KV Path, "Prefill, all

@@ -4,6 +4,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <memory>
 #include <string>
 #include <vector>
 
@@ -49,6 +50,15 @@ struct LayerW {
     const bf16_t *wqkv, *wo, *wgu, *wd, *g_in, *g_post, *g_q, *g_k;
 };
 
+// A stream the library created; shared by a context and its clones and destroyed with
+// the last of them.
+struct OwnedStream {
+    cudaStream_t s = nullptr;
+    ~OwnedStream() {
+        if (s) cudaStreamDestroy(s);
+    }
+};
+
 }  // namespace
 
 namespace qdec {
@@ -72,7 +82,7 @@ struct qdec_ctx {
     const bf16_t* final_norm = nullptr;
     std::vector<LayerW> layers;
     cudaStream_t stream = nullptr;
-    bool own_stream = false;
+    std::shared_ptr<OwnedStream> stream_owner;   // set when the library created `stream`
     cudaStream_t cap_stream = nullptr;   // internal stream used only for graph capture
     int device = 0;
 
@@ -128,7 +138,7 @@ void free_all(qdec_ctx* c) {
         if (p) cudaFree(p);
     if (c->h_pinned) cudaFreeHost(c->h_pinned);
     if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
-    if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
+    c->stream_owner.reset();
 }
 
 int validate_config(const qdec_config* c) {
@@ -374,12 +384,15 @@ int qdec_create(const qdec_config* cfg, const qdec_weights* w, void* cuda_stream
     if (cuda_stream) {
         c->stream = static_cast<cudaStream_t>(cuda_stream);
     } else {
-        cudaError_t e = cudaStreamCreateWithFlags(&c->stream, cudaStreamNonBlocking);
+        auto owner = std::make_shared<OwnedStream>();
+        cudaError_t e = cudaStreamCreateWithFlags(&owner->s, cudaStreamNonBlocking);
         if (e != cudaSuccess) {
+            owner->s = nullptr;
             delete c;
             return fail(QDEC_E_CUDA, "cudaStreamCreate: %s", cudaGetErrorString(e));
         }
-        c->own_stream = true;
+        c->stream = owner->s;
+        c->stream_owner = owner;
     }
     rc = alloc_state(c);
     if (rc == QDEC_OK) rc = build_rope_table(c);
@@ -500,7 +513,7 @@ int qdec_clone(const qdec_ctx* src, qdec_ctx** out) {
     c->final_norm = src->final_norm;
     c->layers = src->layers;
     c->stream = src->stream;
-    c->own_stream = false;
+    c->stream_owner = src->stream_owner;   // keeps a library-created stream alive while any clone uses it
     int rc = alloc_state(c);
     if (rc == QDEC_OK) {
         const Shape& sh = c->sh;

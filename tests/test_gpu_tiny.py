@@ -209,11 +209,15 @@ def test_errors_leave_context_unchanged(model):
     assert e.value.status == -2
     dec.prefill(p.ids, p.audio.cuda(), p.audio_offset)
     assert dec.position == 32
+    with pytest.raises(QdecError) as e:
+        dec.decode_step(-2)
+    assert e.value.status == -1
+    with pytest.raises(QdecError) as e:
+        dec.decode_step(SH.vocab)
+    assert e.value.status == -1
+    assert dec.position == 32
     dec.decode_step(5)
     with pytest.raises(QdecError) as e:
         dec.decode_step(6)                           # slot 33 >= max_seq
     assert e.value.status == -2
-    with pytest.raises(QdecError) as e:
-        dec.decode_step(-2)
-    assert e.value.status == -1
     assert dec.position == 33
