@@ -54,6 +54,27 @@ size_t qdec_op_lm_head_scratch_bytes(int32_t V);
 int qdec_op_lm_head_argmax(const void *E, int32_t V, int32_t H, const float *x, const void *g_final, float eps,
                            float *logits, int32_t *argmax, void *scratch, size_t scratch_bytes, void *stream);
 
+/* Largest vocabulary qdec_op_lm_head_argmax_static accepts. */
+#define QDEC_LM_HEAD_STATIC_MAX_VOCAB 262144
+
+/* The same tied lm_head + argmax as qdec_op_lm_head_argmax, for callers that
+ * cannot let a library allocate device memory: hosts that own all GPU memory
+ * through their own pooling allocator, or real-time threads where cudaMalloc's
+ * implicit device synchronisation and latency are not acceptable.  This call
+ * allocates nothing: the per-block partial maxima and the ticket counter live
+ * in one library-owned static device array of about 64 KB (enough for
+ * QDEC_LM_HEAD_STATIC_MAX_VOCAB rows), which every GPU that loads the library
+ * holds until the process exits.  The paper has no counterpart of this call.
+ * The caller still passes inputs and outputs (as for qdec_op_lm_head_argmax).
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  Each call
+ * clears the ticket counter on `stream` before its kernel.  All calls share
+ * the one array, so calls that overlap on the GPU (different streams, or other
+ * host threads) race and give wrong results: serialise them.  Errors:
+ * INVALID_ARG for a null pointer, H % 8 != 0, or V > the maximum. */
+int qdec_op_lm_head_argmax_static(const void *E, int32_t V, int32_t H, const float *x, const void *g_final, float eps,
+                                  float *logits, int32_t *argmax, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -66,7 +66,10 @@ SIGNATURES = [
     ("qdec_op_attention_prefill", C.c_int, [_VP, _I32, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _I32, _VP]),
     ("qdec_op_lm_head_scratch_bytes", _SZ, [_I32]),
     ("qdec_op_lm_head_argmax", C.c_int, [_VP, _I32, _I32, _VP, _VP, _F, _VP, _VP, _VP, _SZ, _VP]),
+    ("qdec_op_lm_head_argmax_static", C.c_int, [_VP, _I32, _I32, _VP, _VP, _F, _VP, _VP, _VP]),
 ]
+
+LM_HEAD_STATIC_MAX_VOCAB = 262144
 
 
 def load(path: str = LIB_PATH):
@@ -213,6 +216,13 @@ def attention_prefill(Q, T, HQ, HKV, D, max_seq, pos0, k_cache, v_cache, O, impl
 
 def lm_head_scratch_bytes(V: int) -> int:
     return int(load().qdec_op_lm_head_scratch_bytes(V))
+
+
+def lm_head_argmax_static(E, V, H, x, g_final, eps, logits, argmax, stream=None) -> None:
+    """The lm_head + argmax that allocates nothing (library-owned static scratch)."""
+    lib = load()
+    _check(lib.qdec_op_lm_head_argmax_static(_ptr(E), V, H, _ptr(x), _ptr(g_final), float(eps), _ptr(logits),
+                                             _ptr(argmax), _stream_handle(stream)))
 
 
 def lm_head_argmax(E, V, H, x, g_final, eps, logits, argmax, scratch, stream=None) -> None:
