@@ -41,7 +41,8 @@ extern "C" {
 #define QDEC_E_STATE        (-3)  /* decode before prefill, mixed contexts in a batch */
 #define QDEC_E_CUDA         (-4)  /* a CUDA runtime/driver call failed (context may be unusable) */
 #define QDEC_E_OOM          (-5)  /* device or pinned allocation failed */
-#define QDEC_E_TIMEOUT      (-6)  /* a bounded device-side wait gave up (error flag set by a kernel) */
+#define QDEC_E_TIMEOUT      (-6)  /* a bounded device-side wait gave up (error flag set by a kernel);
+                                       the step's outputs and the KV slot it wrote are invalid */
 #define QDEC_E_UNSUPPORTED  (-7)  /* model shape outside what the kernels implement */
 
 /* Model shape.  Qwen3-0.6B: hidden 1024, 28 layers, 16 q heads, 8 kv heads,
@@ -141,8 +142,37 @@ int qdec_read_kv(const qdec_ctx *ctx, int32_t layer, int32_t kind, int32_t pos0,
  * step's input token) to HOST int32.  Synchronises the stream. */
 int qdec_read_history(const qdec_ctx *ctx, int32_t *host_dst, int32_t n);
 
-/* Waits for all work queued by this context. */
+/* Waits for all work queued by this context.  Returns QDEC_E_TIMEOUT if a
+ * queued persistent decode step gave up on a bounded device-side wait. */
 int qdec_sync(const qdec_ctx *ctx);
+
+/* Per-context options. */
+#define QDEC_OPT_DECODE_KERNEL   1   /* which kernels run a decode step: */
+#define QDEC_DECODE_PERSISTENT   0   /*   one persistent kernel per step (default when supported) */
+#define QDEC_DECODE_GRAPH        1   /*   one kernel per operation, replayed as a CUDA graph */
+#define QDEC_OPT_TRACE           2   /* 1: the persistent decode step records a phase trace */
+
+/* Sets an option.  QDEC_OPT_DECODE_KERNEL = QDEC_DECODE_PERSISTENT returns
+ * UNSUPPORTED when the persistent kernel does not cover the shape (head_dim /
+ * GQA group / ffn combination) or the device (cooperative launch with one
+ * CTA per SM).  Clones inherit the setting. */
+int qdec_set_option(qdec_ctx *ctx, int32_t option, int32_t value);
+
+/* Current value of an option, or a negative code. */
+int qdec_get_option(const qdec_ctx *ctx, int32_t option);
+
+/* Phase trace of the last persistent decode step (QDEC_OPT_TRACE = 1): one
+ * row of 11 * n_layers + 8 entries per CTA of the grid (globaltimer ns).
+ * Row layout: [10 l + 2 ph] input ready and [10 l + 2 ph + 1] phase done for
+ * phases ph = 0 QKV, 1 attention, 2 o_proj, 3 gate_up, 4 down_proj of layer
+ * l (0 where the CTA had no work in that phase); [10 NL] start, [10 NL + 1]
+ * lm_head input ready, [10 NL + 2] lm_head done, [10 NL + 3] CTA done;
+ * [10 NL + 4 + l] the producer issued its last copy of layer l;
+ * [11 NL + 5] and [11 NL + 6]: SM clock cycles consumer thread 0 spent
+ * waiting for ring stages and for tagged input vectors.  With
+ * host_dst NULL returns the number of entries; otherwise copies them (HOST,
+ * capacity >= that number), synchronises and returns the number. */
+int qdec_read_trace(const qdec_ctx *ctx, uint64_t *host_dst, int32_t capacity);
 
 /* Frees the context (KV cache, scratch, graphs).  NULL is a no-op. */
 void qdec_destroy(qdec_ctx *ctx);

@@ -20,6 +20,9 @@ STATUS = {-1: "INVALID_ARG", -2: "CAPACITY", -3: "STATE", -4: "CUDA", -5: "OOM",
           -7: "UNSUPPORTED"}
 
 GEMM_STORE_F32, GEMM_ADD_F32, GEMM_SWIGLU_BF16, GEMM_STORE_BF16 = 0, 1, 2, 3
+OPT_DECODE_KERNEL = 1
+OPT_TRACE = 2
+DECODE_PERSISTENT, DECODE_GRAPH = 0, 1
 IMPL_SIMT, IMPL_TCGEN05 = 0, 1
 
 
@@ -58,6 +61,9 @@ SIGNATURES = [
     ("qdec_read_kv", C.c_int, [_VP, _I32, _I32, _I32, _I32, _VP]),
     ("qdec_read_history", C.c_int, [_VP, _VP, _I32]),
     ("qdec_sync", C.c_int, [_VP]),
+    ("qdec_set_option", C.c_int, [_VP, _I32, _I32]),
+    ("qdec_get_option", C.c_int, [_VP, _I32]),
+    ("qdec_read_trace", C.c_int, [_VP, _VP, _I32]),
     ("qdec_destroy", None, [_VP]),
     ("qdec_strerror", C.c_char_p, [C.c_int]),
     ("qdec_last_error", C.c_char_p, []),
@@ -194,6 +200,31 @@ class Decoder:
 
     def sync(self) -> None:
         _check(self.lib.qdec_sync(self.handle))
+
+    def set_trace(self, on: bool) -> None:
+        _check(self.lib.qdec_set_option(self.handle, OPT_TRACE, 1 if on else 0))
+
+    def read_trace(self) -> np.ndarray:
+        """[grid, 11 * n_layers + 8] trace of the last persistent step (see qdec_read_trace)."""
+        n = self.lib.qdec_read_trace(self.handle, None, 0)
+        if n < 0:
+            _check(n)
+        out = np.zeros(n, dtype=np.uint64)
+        r = self.lib.qdec_read_trace(self.handle, _ptr(out), n)
+        if r < 0:
+            _check(r)
+        return out.reshape(-1, 11 * self.shape.n_layers + 8)
+
+    @property
+    def decode_kernel(self) -> int:
+        r = self.lib.qdec_get_option(self.handle, OPT_DECODE_KERNEL)
+        if r < 0:
+            _check(r)
+        return r
+
+    @decode_kernel.setter
+    def decode_kernel(self, value: int) -> None:
+        _check(self.lib.qdec_set_option(self.handle, OPT_DECODE_KERNEL, int(value)))
 
 
 def kernel_launches() -> int:

@@ -117,6 +117,20 @@ struct qdec_ctx {
     cudaGraphExec_t decode_exec = nullptr;
     uint64_t decode_graph_kernels = 0;   // kernel nodes in decode_exec
 
+    // persistent single-kernel decode step
+    int decode_kernel = QDEC_DECODE_PERSISTENT;
+    bool persistent_ok = false;
+    DecodeLaunch dp;
+    DecodeLayer* d_layers = nullptr;
+    unsigned long long *ll_x = nullptr, *ll_qkv = nullptr, *ll_o = nullptr, *ll_h = nullptr;
+    float* attn_part = nullptr;
+    unsigned int* attn_count = nullptr;
+    ArgMax* am_part = nullptr;
+    unsigned int* am_count = nullptr;
+    uint32_t epoch = 0;
+    int* d_err = nullptr;                // d_argmax + 1
+    unsigned long long* d_trace = nullptr;   // phase trace of the persistent step (QDEC_OPT_TRACE)
+
     size_t kv_layer_stride() const { return (size_t)2 * sh.HKV * sh.max_seq * sh.D; }
     bf16_t* k_cache(int l) { return kv + (size_t)l * kv_layer_stride(); }
     bf16_t* v_cache(int l) { return kv + (size_t)l * kv_layer_stride() + (size_t)sh.HKV * sh.max_seq * sh.D; }
@@ -133,7 +147,9 @@ void free_all(qdec_ctx* c) {
     if (c->decode_exec) cudaGraphExecDestroy(c->decode_exec);
     void* ptrs[] = {c->kv, c->rope, c->d_hist, c->d_pos, c->d_zero, c->d_argmax, c->d_x, c->d_qkv, c->d_q,
                     c->d_attn, c->d_h, c->d_logits, c->d_part_ml, c->d_part_o, c->d_lm_scratch, c->p_X,
-                    c->p_qkv, c->p_Xn, c->p_Q, c->p_O, c->p_H, c->p_ids, c->p_audio};
+                    c->p_qkv, c->p_Xn, c->p_Q, c->p_O, c->p_H, c->p_ids, c->p_audio, c->d_layers, c->ll_x,
+                    c->ll_qkv, c->ll_o, c->ll_h, c->attn_part, c->attn_count, c->am_part, c->am_count,
+                    c->d_trace};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     if (c->h_pinned) cudaFreeHost(c->h_pinned);
@@ -163,6 +179,8 @@ int validate_config(const qdec_config* c) {
     return QDEC_OK;
 }
 
+int alloc_persistent(qdec_ctx* c);
+
 int alloc_state(qdec_ctx* c) {
     const Shape& sh = c->sh;
     CK(cudaGetDevice(&c->device));
@@ -173,10 +191,11 @@ int alloc_state(qdec_ctx* c) {
     CK(dalloc(&c->d_hist, (size_t)sh.max_seq));
     CK(dalloc(&c->d_pos, 1));
     CK(dalloc(&c->d_zero, 1));
-    CK(dalloc(&c->d_argmax, 1));
+    CK(dalloc(&c->d_argmax, 4));   // [0] argmax, [1] error word of the persistent step
+    c->d_err = c->d_argmax + 1;
     CK(cudaMemset(c->d_pos, 0, sizeof(int)));
     CK(cudaMemset(c->d_zero, 0, sizeof(int)));
-    CK(cudaMemset(c->d_argmax, 0, sizeof(int)));
+    CK(cudaMemset(c->d_argmax, 0, 4 * sizeof(int)));
     CK(dalloc(&c->d_x, sh.H));
     CK(dalloc(&c->d_qkv, sh.qkv_rows()));
     CK(dalloc(&c->d_q, (size_t)sh.HQ * sh.D));
@@ -191,6 +210,43 @@ int alloc_state(qdec_ctx* c) {
     CK(cudaMemset(c->d_lm_scratch, 0, lm));
     CK(cudaMallocHost(reinterpret_cast<void**>(&c->h_pinned), 64 * sizeof(int)));
     c->h_pinned_cap = 64;
+    return alloc_persistent(c);
+}
+
+// Buffers of the persistent decode kernel; leaves persistent_ok false (and the graph
+// path selected) when the kernel does not cover the shape or the device.
+int alloc_persistent(qdec_ctx* c) {
+    const Shape& sh = c->sh;
+    cudaError_t e = decode_persistent_plan(sh, c->device, &c->dp);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        c->persistent_ok = false;
+        c->decode_kernel = QDEC_DECODE_GRAPH;
+        return QDEC_OK;
+    }
+    CK(dalloc(&c->d_layers, (size_t)sh.NL));
+    std::vector<DecodeLayer> hl(sh.NL);
+    for (int l = 0; l < sh.NL; ++l) {
+        const LayerW& w = c->layers[l];
+        hl[l] = DecodeLayer{w.wqkv, w.wo, w.wgu, w.wd, w.g_in, w.g_post, w.g_q, w.g_k, c->k_cache(l), c->v_cache(l)};
+    }
+    CK(cudaMemcpy(c->d_layers, hl.data(), hl.size() * sizeof(DecodeLayer), cudaMemcpyHostToDevice));
+    CK(dalloc(&c->ll_x, (size_t)sh.H));
+    CK(dalloc(&c->ll_qkv, (size_t)sh.qkv_rows()));
+    CK(dalloc(&c->ll_o, (size_t)sh.HQ * sh.D));
+    CK(dalloc(&c->ll_h, (size_t)sh.F));
+    CK(cudaMemset(c->ll_x, 0, (size_t)sh.H * 8));
+    CK(cudaMemset(c->ll_qkv, 0, (size_t)sh.qkv_rows() * 8));
+    CK(cudaMemset(c->ll_o, 0, (size_t)sh.HQ * sh.D * 8));
+    CK(cudaMemset(c->ll_h, 0, (size_t)sh.F * 8));
+    CK(dalloc(&c->attn_part, (size_t)sh.HQ * c->dp.max_chunks * (sh.D + 2)));
+    CK(dalloc(&c->attn_count, (size_t)sh.NL * sh.HKV));
+    CK(cudaMemset(c->attn_count, 0, (size_t)sh.NL * sh.HKV * sizeof(unsigned int)));
+    CK(dalloc(&c->am_part, (size_t)c->dp.grid));
+    CK(dalloc(&c->am_count, 1));
+    CK(cudaMemset(c->am_count, 0, sizeof(unsigned int)));
+    c->persistent_ok = true;
+    c->decode_kernel = QDEC_DECODE_PERSISTENT;
     return QDEC_OK;
 }
 
@@ -330,11 +386,59 @@ int ensure_decode_graph(qdec_ctx* c) {
 
 // Queues one decode step (no host synchronisation).
 int enqueue_decode_step(qdec_ctx* c, int token) {
+    if (c->decode_kernel == QDEC_DECODE_PERSISTENT) {
+        const Shape& sh = c->sh;
+        DecodeParams p{};
+        p.layers = c->d_layers;
+        p.embed = c->embed;
+        p.final_norm = c->final_norm;
+        p.rope = c->rope;
+        p.H = sh.H; p.NL = sh.NL; p.HQ = sh.HQ; p.HKV = sh.HKV; p.D = sh.D; p.F = sh.F; p.V = sh.V;
+        p.max_seq = sh.max_seq;
+        p.eps = sh.eps;
+        p.pos = c->position;
+        p.token = token;
+        p.epoch = ++c->epoch;
+        decode_persistent_chunks(c->dp, c->position + 1, &p.n_chunks, &p.chunk);
+        p.argmax = c->d_argmax;
+        p.pos_out = c->d_pos;
+        p.history = c->d_hist;
+        p.logits = c->d_logits;
+        p.ll_x = c->ll_x; p.ll_qkv = c->ll_qkv; p.ll_o = c->ll_o; p.ll_h = c->ll_h;
+        p.attn_part = c->attn_part;
+        p.attn_count = c->attn_count;
+        p.am_part = c->am_part;
+        p.am_count = c->am_count;
+        p.err = c->d_err;
+        p.trace = c->d_trace;
+        if (p.trace)
+            CK(cudaMemsetAsync(p.trace, 0, (size_t)c->dp.grid * (11 * sh.NL + 8) * sizeof(unsigned long long),
+                               c->stream));
+        CK(launch_decode_persistent(p, c->dp, c->stream));
+        count_launches(1);
+        return QDEC_OK;
+    }
     int rc = ensure_decode_graph(c);
     if (rc != QDEC_OK) return rc;
     CK(launch_embed_token(c->embed, token, c->d_argmax, c->d_pos, c->sh.H, c->d_x, c->d_hist, c->stream));
     CK(cudaGraphLaunch(c->decode_exec, c->stream));
     count_launches(1 + c->decode_graph_kernels);
+    return QDEC_OK;
+}
+
+// Reads the step's argmax and the persistent kernel's error word into the pinned staging
+// (slots [s], [s+1]) and waits.  A device-side timeout is reported as QDEC_E_TIMEOUT and
+// the error word is cleared.
+int sync_status(qdec_ctx* c, int s, int* argmax) {
+    CK(cudaMemcpyAsync(&c->h_pinned[s], c->d_argmax, 2 * sizeof(int), cudaMemcpyDeviceToHost, c->stream));
+    CK(cudaStreamSynchronize(c->stream));
+    if (c->h_pinned[s + 1] != 0) {
+        const int code = c->h_pinned[s + 1];
+        CK(cudaMemsetAsync(c->d_err, 0, sizeof(int), c->stream));
+        CK(cudaStreamSynchronize(c->stream));
+        return fail(QDEC_E_TIMEOUT, "decode kernel gave up waiting (device error code %d)", code);
+    }
+    if (argmax) *argmax = c->h_pinned[s];
     return QDEC_OK;
 }
 
@@ -464,11 +568,7 @@ int qdec_decode_step(qdec_ctx* c, int32_t token, float* logits_out, int32_t* arg
     c->position += 1;
     rc = copy_logits_out(c, logits_out);
     if (rc != QDEC_OK) return rc;
-    if (argmax_out) {
-        CK(cudaMemcpyAsync(&c->h_pinned[0], c->d_argmax, sizeof(int), cudaMemcpyDeviceToHost, c->stream));
-        CK(cudaStreamSynchronize(c->stream));
-        *argmax_out = c->h_pinned[0];
-    }
+    if (argmax_out) return sync_status(c, 0, argmax_out);
     return QDEC_OK;
 }
 
@@ -491,11 +591,9 @@ int qdec_decode_step_batch(qdec_ctx* const* ctxs, int32_t n, const int32_t* toke
         c->position += 1;
         if (logits_out) CK(cudaMemcpyAsync(logits_out + (size_t)i * V, c->d_logits, (size_t)V * sizeof(float),
                                            cudaMemcpyDefault, c->stream));
-        if (argmax_out)
-            CK(cudaMemcpyAsync(&c->h_pinned[2], c->d_argmax, sizeof(int), cudaMemcpyDeviceToHost, c->stream));
         if (argmax_out) {
-            CK(cudaStreamSynchronize(c->stream));
-            argmax_out[i] = c->h_pinned[2];
+            rc = sync_status(c, 2, &argmax_out[i]);
+            if (rc != QDEC_OK) return rc;
         }
     }
     for (int i = 0; i < n; ++i) CK(cudaStreamSynchronize(ctxs[i]->stream));
@@ -542,6 +640,7 @@ int qdec_clone(const qdec_ctx* src, qdec_ctx** out) {
     }
     c->position = src->position;
     c->prefilled = src->prefilled;
+    if (c->persistent_ok) c->decode_kernel = src->decode_kernel;
     *out = c;
     return QDEC_OK;
 }
@@ -576,8 +675,39 @@ int qdec_read_history(const qdec_ctx* c, int32_t* host_dst, int32_t n) {
 
 int qdec_sync(const qdec_ctx* c) {
     if (!c) return fail(QDEC_E_INVALID_ARG, "null context");
-    CK(cudaStreamSynchronize(c->stream));
+    return sync_status(const_cast<qdec_ctx*>(c), 4, nullptr);
+}
+
+int qdec_set_option(qdec_ctx* c, int32_t option, int32_t value) {
+    if (!c) return fail(QDEC_E_INVALID_ARG, "null context");
+    if (option == QDEC_OPT_TRACE) {
+        if (value != 0 && value != 1) return fail(QDEC_E_INVALID_ARG, "QDEC_OPT_TRACE takes 0 or 1");
+        if (value == 1 && !c->persistent_ok) return fail(QDEC_E_UNSUPPORTED, "no persistent decode kernel to trace");
+        if (value == 1 && !c->d_trace) {
+            const size_t n = (size_t)c->dp.grid * (11 * c->sh.NL + 8);
+            CK(dalloc(&c->d_trace, n));
+            CK(cudaMemset(c->d_trace, 0, n * sizeof(unsigned long long)));
+        } else if (value == 0 && c->d_trace) {
+            CK(cudaStreamSynchronize(c->stream));
+            cudaFree(c->d_trace);
+            c->d_trace = nullptr;
+        }
+        return QDEC_OK;
+    }
+    if (option != QDEC_OPT_DECODE_KERNEL) return fail(QDEC_E_INVALID_ARG, "unknown option %d", option);
+    if (value != QDEC_DECODE_PERSISTENT && value != QDEC_DECODE_GRAPH)
+        return fail(QDEC_E_INVALID_ARG, "bad value %d for QDEC_OPT_DECODE_KERNEL", value);
+    if (value == QDEC_DECODE_PERSISTENT && !c->persistent_ok)
+        return fail(QDEC_E_UNSUPPORTED, "the persistent decode kernel does not cover this shape or device");
+    c->decode_kernel = value;
     return QDEC_OK;
+}
+
+int qdec_get_option(const qdec_ctx* c, int32_t option) {
+    if (!c) return fail(QDEC_E_INVALID_ARG, "null context");
+    if (option == QDEC_OPT_TRACE) return c->d_trace ? 1 : 0;
+    if (option != QDEC_OPT_DECODE_KERNEL) return fail(QDEC_E_INVALID_ARG, "unknown option %d", option);
+    return c->decode_kernel;
 }
 
 void qdec_destroy(qdec_ctx* c) {
@@ -585,6 +715,17 @@ void qdec_destroy(qdec_ctx* c) {
     if (c->stream) cudaStreamSynchronize(c->stream);
     free_all(c);
     delete c;
+}
+
+int qdec_read_trace(const qdec_ctx* c, uint64_t* host_dst, int32_t capacity) {
+    if (!c) return fail(QDEC_E_INVALID_ARG, "null context");
+    if (!c->d_trace) return fail(QDEC_E_STATE, "tracing is off (QDEC_OPT_TRACE)");
+    const int n = c->dp.grid * (11 * c->sh.NL + 8);
+    if (!host_dst) return n;
+    if (capacity < n) return fail(QDEC_E_INVALID_ARG, "trace needs %d entries", n);
+    CK(cudaMemcpyAsync(host_dst, c->d_trace, (size_t)n * sizeof(uint64_t), cudaMemcpyDeviceToHost, c->stream));
+    CK(cudaStreamSynchronize(c->stream));
+    return n;
 }
 
 const char* qdec_strerror(int status) {

@@ -103,4 +103,46 @@ size_t lm_head_scratch_bytes(int V);
 cudaError_t launch_lm_head_argmax(const bf16_t* E, int V, int H, const float* x, const bf16_t* g_final,
                                   float eps, float* logits, int* argmax, void* scratch, cudaStream_t s);
 
+// ---------------------------------------------------------------- persistent decode
+struct DecodeLayer {
+    const bf16_t *wqkv, *wo, *wgu, *wd, *g_in, *g_post, *g_q, *g_k;
+    bf16_t *kc, *vc;   // this layer's K and V cache [HKV][max_seq][D]
+};
+
+struct DecodeParams {
+    const DecodeLayer* layers;          // device [NL]
+    const bf16_t* embed;
+    const bf16_t* final_norm;
+    const float2* rope;                 // [max_seq][D/2] (cos, sin)
+    int H, NL, HQ, HKV, D, F, V, max_seq;
+    float eps;
+    int pos;                            // position of the new token
+    int token;                          // >= 0, or -1 for *argmax
+    uint32_t epoch;                     // distinct per launch for one context's buffers
+    int n_chunks, chunk;                // attention split of [0, pos + 1)
+    int nslot;                          // filled by the launcher
+    int* argmax;                        // in: previous argmax; out: this step's
+    int* pos_out;                       // set to pos + 1 at the end of the step
+    int* history;                       // [max_seq]
+    float* logits;                      // [V]
+    unsigned long long *ll_x, *ll_qkv, *ll_o, *ll_h;   // tagged vectors {tag, fp32}
+    float* attn_part;                   // [HQ][max_chunks][D + 2]
+    unsigned int* attn_count;           // [NL * HKV], zero between steps
+    ArgMax* am_part;                    // [grid]
+    unsigned int* am_count;             // zero between steps
+    int* err;                           // 0, or the first error code of the step
+    unsigned long long* trace;          // optional [grid][11 NL + 4] globaltimer stamps, or null
+};
+
+struct DecodeLaunch {
+    const void* fn = nullptr;
+    int grid = 0, threads = 0, smem = 0, nslot = 0, max_chunks = 1;
+};
+
+// Chooses the instantiation, ring depth and grid for `sh` on `device`; cudaErrorNotSupported
+// when the persistent kernel does not cover the shape or the device.
+cudaError_t decode_persistent_plan(const Shape& sh, int device, DecodeLaunch* out);
+void decode_persistent_chunks(const DecodeLaunch& cfg, int L, int* n_chunks, int* chunk);
+cudaError_t launch_decode_persistent(const DecodeParams& p, const DecodeLaunch& cfg, cudaStream_t s);
+
 }  // namespace qdec

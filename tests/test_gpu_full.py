@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from qwen3_prefill_kv_gb300 import synth
-from qwen3_prefill_kv_gb300._lib import Decoder
+from qwen3_prefill_kv_gb300._lib import Decoder, DECODE_PERSISTENT, DECODE_GRAPH
 
 import _harness as H
 
@@ -56,6 +56,33 @@ def test_teacher_forced_workload(full, name):
     kv_prompt = p.ids.numpy().copy()
     mask = np.ones(kv_prompt.size, bool); mask[wl.audio_offset:wl.audio_offset + wl.n_audio] = False
     assert np.array_equal(hist[:wl.n_prompt][mask], kv_prompt[mask])
+
+
+def test_persistent_and_graph_decode_agree(full):
+    """The persistent single-kernel step and the per-op graph step compute the same
+    function; with different summation orders they agree to fp32 rounding."""
+    w, wd, orc = full
+    wl = synth.WORKLOADS["qwen3_asr_30s"]
+    p = synth.make_prompt(wl, seed=1)
+    a = Decoder(SH, wd, max_seq=wl.max_seq)
+    b = Decoder(SH, wd, max_seq=wl.max_seq)
+    assert a.decode_kernel == DECODE_PERSISTENT
+    b.decode_kernel = DECODE_GRAPH
+    la = torch.empty(SH.vocab, device="cuda"); lb = torch.empty(SH.vocab, device="cuda")
+    ta = a.prefill(p.ids, p.audio.cuda(), p.audio_offset)
+    b.prefill(p.ids, p.audio.cuda(), p.audio_offset)
+    for t in synth.make_tokens(SH.vocab, 12, seed=7).tolist():
+        a.decode_step(t, logits=la)
+        b.decode_step(t, logits=lb)
+        ga, gb = la.cpu().double().numpy(), lb.cpu().double().numpy()
+        assert np.abs(ga - gb).max() <= 1e-3 * np.abs(gb).max()
+    f = lambda u: (u.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    for l in (0, 13, 27):
+        for kind in (0, 1):
+            ka = f(a.read_kv(l, kind, 0, wl.n_prompt + 12))
+            kb = f(b.read_kv(l, kind, 0, wl.n_prompt + 12))
+            assert np.array_equal(ka[:, :wl.n_prompt], kb[:, :wl.n_prompt])     # same prefill kernels
+            assert np.abs(ka - kb).max() <= 2e-2 * np.abs(kb).max()
 
 
 @pytest.mark.slow

@@ -7,7 +7,7 @@ import torch
 
 import oracle
 from qwen3_prefill_kv_gb300 import synth
-from qwen3_prefill_kv_gb300._lib import Decoder, QdecError
+from qwen3_prefill_kv_gb300._lib import Decoder, QdecError, DECODE_PERSISTENT, DECODE_GRAPH
 
 import _harness as H
 
@@ -38,18 +38,33 @@ LAYOUTS = [(12, 8, 12, 16),     # the tiny workload: 32 positions, 16 steps
            (10, 6, 0, 4),       # audio ends at the last position
            (40, 0, 0, 4),       # text only
            (1, 0, 0, 3),        # a single-token prompt
-           (3, 130, 2, 2)]      # 135 positions
+           (3, 130, 2, 2),      # 135 positions
+           (3, 590, 7, 4)]      # 600 positions: decode attention split over several key chunks
 
 
+@pytest.mark.parametrize("kernel", [DECODE_PERSISTENT, DECODE_GRAPH], ids=["persistent", "graph"])
 @pytest.mark.parametrize("layout", LAYOUTS)
-def test_teacher_forced_logits(model, layout):
+def test_teacher_forced_logits(model, layout, kernel):
     w, wd, orc = model
     n_prefix, n_audio, n_suffix, steps = layout
     p = _prompt(n_prefix, n_audio, n_suffix)
     dec = Decoder(SH, wd, max_seq=p.ids.numel() + steps)
+    dec.decode_kernel = kernel
+    assert dec.decode_kernel == kernel
     res = H.teacher_forced(dec, orc, p, steps)
     H.assert_step_parity(res, f"tiny {layout}")
     assert dec.position == p.ids.numel() + steps
+
+
+def test_persistent_kernel_is_the_default(model):
+    w, wd, orc = model
+    dec = Decoder(SH, wd, max_seq=40)
+    assert dec.decode_kernel == DECODE_PERSISTENT
+    assert dec.clone().decode_kernel == DECODE_PERSISTENT
+    dec.decode_kernel = DECODE_GRAPH
+    assert dec.clone().decode_kernel == DECODE_GRAPH
+    with pytest.raises(QdecError):
+        dec.decode_kernel = 7
 
 
 def test_gain_jitter(model_jitter):
