@@ -151,6 +151,10 @@ int qdec_sync(const qdec_ctx *ctx);
 #define QDEC_DECODE_PERSISTENT   0   /*   one persistent kernel per step (default when supported) */
 #define QDEC_DECODE_GRAPH        1   /*   one kernel per operation, replayed as a CUDA graph */
 #define QDEC_OPT_TRACE           2   /* 1: the persistent decode step records a phase trace */
+#define QDEC_OPT_PREFILL_IMPL    3   /* prefill projections and attention on: */
+#define QDEC_PREFILL_TCGEN05     0   /*   tcgen05 tensor cores, TMA-fed (default, where the shape
+                                            allows: attention needs head_dim 128) */
+#define QDEC_PREFILL_SIMT        1   /*   CUDA cores */
 
 /* Sets an option.  QDEC_OPT_DECODE_KERNEL = QDEC_DECODE_PERSISTENT returns
  * UNSUPPORTED when the persistent kernel does not cover the shape (head_dim /

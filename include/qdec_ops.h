@@ -31,6 +31,11 @@ extern "C" {
 int qdec_op_gemm(const void *A, int32_t lda, const void *W, int32_t M, int32_t N, int32_t K, int32_t mode,
                  int32_t up_off, void *C, int32_t ldc, int32_t impl, void *stream);
 
+/* Synchronises the device and reports whether a tensor-core kernel launched
+ * through these entry points gave up on a bounded wait since the last call:
+ * QDEC_OK, or QDEC_E_TIMEOUT (the flag is then cleared). */
+int qdec_op_device_error(void);
+
 /* Causal GQA attention for T query rows at positions pos0..pos0+T-1 over
  * cache keys [0, pos0 + T): Q bf16 [T, HQ, D]; k_cache / v_cache bf16
  * [HKV][max_seq][D]; O bf16 [T, HQ * D] ("Qwen3ASR ncnn多平台移植" §5, the

@@ -22,6 +22,8 @@ STATUS = {-1: "INVALID_ARG", -2: "CAPACITY", -3: "STATE", -4: "CUDA", -5: "OOM",
 GEMM_STORE_F32, GEMM_ADD_F32, GEMM_SWIGLU_BF16, GEMM_STORE_BF16 = 0, 1, 2, 3
 OPT_DECODE_KERNEL = 1
 OPT_TRACE = 2
+OPT_PREFILL_IMPL = 3
+PREFILL_TCGEN05, PREFILL_SIMT = 0, 1
 DECODE_PERSISTENT, DECODE_GRAPH = 0, 1
 IMPL_SIMT, IMPL_TCGEN05 = 0, 1
 
@@ -69,6 +71,7 @@ SIGNATURES = [
     ("qdec_last_error", C.c_char_p, []),
     ("qdec_kernel_launches", C.c_uint64, []),
     ("qdec_op_gemm", C.c_int, [_VP, _I32, _VP, _I32, _I32, _I32, _I32, _I32, _VP, _I32, _I32, _VP]),
+    ("qdec_op_device_error", C.c_int, []),
     ("qdec_op_attention_prefill", C.c_int, [_VP, _I32, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _I32, _VP]),
     ("qdec_op_lm_head_scratch_bytes", _SZ, [_I32]),
     ("qdec_op_lm_head_argmax", C.c_int, [_VP, _I32, _I32, _VP, _VP, _F, _VP, _VP, _VP, _SZ, _VP]),
@@ -201,6 +204,15 @@ class Decoder:
     def sync(self) -> None:
         _check(self.lib.qdec_sync(self.handle))
 
+    def set_option(self, option: int, value: int) -> None:
+        _check(self.lib.qdec_set_option(self.handle, int(option), int(value)))
+
+    def get_option(self, option: int) -> int:
+        r = self.lib.qdec_get_option(self.handle, int(option))
+        if r < 0:
+            _check(r)
+        return r
+
     def set_trace(self, on: bool) -> None:
         _check(self.lib.qdec_set_option(self.handle, OPT_TRACE, 1 if on else 0))
 
@@ -237,6 +249,11 @@ def gemm(A, W, M, N, K, mode, C_out, lda=None, ldc=None, up_off=0, impl=IMPL_SIM
     lib = load()
     _check(lib.qdec_op_gemm(_ptr(A), lda if lda is not None else K, _ptr(W), M, N, K, mode, up_off, _ptr(C_out),
                             ldc if ldc is not None else N, impl, _stream_handle(stream)))
+
+
+def device_error() -> None:
+    """Raises QdecError(TIMEOUT) if a tensor-core kernel gave up on a bounded wait."""
+    _check(load().qdec_op_device_error())
 
 
 def attention_prefill(Q, T, HQ, HKV, D, max_seq, pos0, k_cache, v_cache, O, impl=IMPL_SIMT, stream=None) -> None:

@@ -130,6 +130,7 @@ struct qdec_ctx {
     uint32_t epoch = 0;
     int* d_err = nullptr;                // d_argmax + 1
     unsigned long long* d_trace = nullptr;   // phase trace of the persistent step (QDEC_OPT_TRACE)
+    int prefill_gemm = QDEC_PREFILL_TCGEN05;
 
     size_t kv_layer_stride() const { return (size_t)2 * sh.HKV * sh.max_seq * sh.D; }
     bf16_t* k_cache(int l) { return kv + (size_t)l * kv_layer_stride(); }
@@ -316,6 +317,14 @@ int copy_logits_out(qdec_ctx* c, float* dst) {
 
 constexpr uint64_t kPrefillKernelsPerLayer = 8;
 
+// Prefill GEMM: tcgen05 kernel where the shape allows it (and it is selected), else CUDA cores.
+cudaError_t prefill_gemm(const qdec_ctx* c, const bf16_t* A, int lda, const bf16_t* W, int M, int N, int K, int mode,
+                         int up_off, float* Cf, bf16_t* Cb, int ldc, cudaStream_t s) {
+    if (c->prefill_gemm == QDEC_PREFILL_TCGEN05 && gemm_tc_supported(N, K, mode, lda))
+        return launch_gemm_tc(A, lda, W, M, N, K, mode, up_off, Cf, Cb, ldc, s);
+    return launch_gemm_simt(A, lda, W, M, N, K, mode, up_off, Cf, Cb, ldc, s);
+}
+
 // One layer of the prefill over T rows starting at position 0.
 int prefill_layer(qdec_ctx* c, int l, int T) {
     const Shape& sh = c->sh;
@@ -323,15 +332,18 @@ int prefill_layer(qdec_ctx* c, int l, int T) {
     cudaStream_t s = c->stream;
     const int qd = sh.HQ * sh.D;
     CK(launch_rmsnorm_bf16(c->p_X, T, sh.H, w.g_in, sh.eps, c->p_Xn, s));
-    CK(launch_gemm_simt(c->p_Xn, sh.H, w.wqkv, T, sh.qkv_rows(), sh.H, GEMM_STORE_F32, 0, c->p_qkv, nullptr,
+    CK(prefill_gemm(c, c->p_Xn, sh.H, w.wqkv, T, sh.qkv_rows(), sh.H, GEMM_STORE_F32, 0, c->p_qkv, nullptr,
                         sh.qkv_rows(), s));
     CK(launch_qk_norm_rope_append(c->p_qkv, T, sh, c->d_zero, w.g_q, w.g_k, c->rope, c->p_Q, nullptr,
                                   c->k_cache(l), c->v_cache(l), s));
-    CK(launch_attention_prefill_simt(c->p_Q, T, sh, 0, c->k_cache(l), c->v_cache(l), c->p_O, s));
-    CK(launch_gemm_simt(c->p_O, qd, w.wo, T, sh.H, qd, GEMM_ADD_F32, 0, c->p_X, nullptr, sh.H, s));
+    if (c->prefill_gemm == QDEC_PREFILL_TCGEN05 && attention_tc_supported(sh))
+        CK(launch_attention_prefill_tc(c->p_Q, T, sh, 0, c->k_cache(l), c->v_cache(l), c->p_O, s));
+    else
+        CK(launch_attention_prefill_simt(c->p_Q, T, sh, 0, c->k_cache(l), c->v_cache(l), c->p_O, s));
+    CK(prefill_gemm(c, c->p_O, qd, w.wo, T, sh.H, qd, GEMM_ADD_F32, 0, c->p_X, nullptr, sh.H, s));
     CK(launch_rmsnorm_bf16(c->p_X, T, sh.H, w.g_post, sh.eps, c->p_Xn, s));
-    CK(launch_gemm_simt(c->p_Xn, sh.H, w.wgu, T, sh.F, sh.H, GEMM_SWIGLU_BF16, sh.F, nullptr, c->p_H, sh.F, s));
-    CK(launch_gemm_simt(c->p_H, sh.F, w.wd, T, sh.H, sh.F, GEMM_ADD_F32, 0, c->p_X, nullptr, sh.H, s));
+    CK(prefill_gemm(c, c->p_Xn, sh.H, w.wgu, T, sh.F, sh.H, GEMM_SWIGLU_BF16, sh.F, nullptr, c->p_H, sh.F, s));
+    CK(prefill_gemm(c, c->p_H, sh.F, w.wd, T, sh.H, sh.F, GEMM_ADD_F32, 0, c->p_X, nullptr, sh.H, s));
     return QDEC_OK;
 }
 
@@ -438,6 +450,9 @@ int sync_status(qdec_ctx* c, int s, int* argmax) {
         CK(cudaStreamSynchronize(c->stream));
         return fail(QDEC_E_TIMEOUT, "decode kernel gave up waiting (device error code %d)", code);
     }
+    const int tc = tc_error_read_and_clear(), fa = fa_error_read_and_clear();
+    if (tc > 0 || fa > 0)
+        return fail(QDEC_E_TIMEOUT, "a tensor-core prefill kernel gave up waiting (codes %d, %d)", tc, fa);
     if (argmax) *argmax = c->h_pinned[s];
     return QDEC_OK;
 }
@@ -552,11 +567,7 @@ int qdec_prefill(qdec_ctx* c, const int32_t* ids, int32_t n_ids, const void* aud
     c->prefilled = true;
     rc = copy_logits_out(c, logits_out);
     if (rc != QDEC_OK) return rc;
-    if (argmax_out) {
-        CK(cudaMemcpyAsync(&c->h_pinned[0], c->d_argmax, sizeof(int), cudaMemcpyDeviceToHost, s));
-        CK(cudaStreamSynchronize(s));
-        *argmax_out = c->h_pinned[0];
-    }
+    if (argmax_out) return sync_status(c, 0, argmax_out);
     return QDEC_OK;
 }
 
@@ -641,6 +652,7 @@ int qdec_clone(const qdec_ctx* src, qdec_ctx** out) {
     c->position = src->position;
     c->prefilled = src->prefilled;
     if (c->persistent_ok) c->decode_kernel = src->decode_kernel;
+    c->prefill_gemm = src->prefill_gemm;
     *out = c;
     return QDEC_OK;
 }
@@ -680,6 +692,12 @@ int qdec_sync(const qdec_ctx* c) {
 
 int qdec_set_option(qdec_ctx* c, int32_t option, int32_t value) {
     if (!c) return fail(QDEC_E_INVALID_ARG, "null context");
+    if (option == QDEC_OPT_PREFILL_IMPL) {
+        if (value != QDEC_PREFILL_TCGEN05 && value != QDEC_PREFILL_SIMT)
+            return fail(QDEC_E_INVALID_ARG, "bad value %d for QDEC_OPT_PREFILL_IMPL", value);
+        c->prefill_gemm = value;
+        return QDEC_OK;
+    }
     if (option == QDEC_OPT_TRACE) {
         if (value != 0 && value != 1) return fail(QDEC_E_INVALID_ARG, "QDEC_OPT_TRACE takes 0 or 1");
         if (value == 1 && !c->persistent_ok) return fail(QDEC_E_UNSUPPORTED, "no persistent decode kernel to trace");
@@ -706,6 +724,7 @@ int qdec_set_option(qdec_ctx* c, int32_t option, int32_t value) {
 int qdec_get_option(const qdec_ctx* c, int32_t option) {
     if (!c) return fail(QDEC_E_INVALID_ARG, "null context");
     if (option == QDEC_OPT_TRACE) return c->d_trace ? 1 : 0;
+    if (option == QDEC_OPT_PREFILL_IMPL) return c->prefill_gemm;
     if (option != QDEC_OPT_DECODE_KERNEL) return fail(QDEC_E_INVALID_ARG, "unknown option %d", option);
     return c->decode_kernel;
 }

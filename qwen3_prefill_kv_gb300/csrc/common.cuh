@@ -71,6 +71,15 @@ enum GemmMode { GEMM_STORE_F32 = 0, GEMM_ADD_F32 = 1, GEMM_SWIGLU_BF16 = 2, GEMM
 cudaError_t launch_gemm_simt(const bf16_t* A, int lda, const bf16_t* W, int M, int N, int K, int mode,
                              int up_off, float* Cf, bf16_t* Cb, int ldc, cudaStream_t s);
 
+// The same GEMM on the tcgen05 tensor cores (TMA-fed, TMEM accumulator).  Needs K % 64 == 0,
+// lda % 8 == 0, N % 128 == 0 (SwiGLU: N % 64 == 0) and 16-byte aligned A, W.
+bool gemm_tc_supported(int N, int K, int mode, int lda);
+cudaError_t launch_gemm_tc(const bf16_t* A, int lda, const bf16_t* W, int M, int N, int K, int mode, int up_off,
+                           float* Cf, bf16_t* Cb, int ldc, cudaStream_t s);
+// First timeout code recorded by a tensor-core kernel since the last call (0 = none);
+// synchronous, clears the flag.
+int tc_error_read_and_clear();
+
 // Per-head RMSNorm + NeoX RoPE on q and k, V copy, KV append at slots pos0 + t.
 // qkv fp32 [T, (HQ+2HKV) D]; q_out: bf16 [T, HQ, D] (q_bf16) or fp32 (q_f32).
 cudaError_t launch_qk_norm_rope_append(const float* qkv, int T, const Shape& sh, const int* pos0,
@@ -82,6 +91,12 @@ cudaError_t launch_qk_norm_rope_append(const float* qkv, int T, const Shape& sh,
 cudaError_t launch_attention_prefill_simt(const bf16_t* Q, int T, const Shape& sh, int pos0,
                                           const bf16_t* k_cache, const bf16_t* v_cache,
                                           bf16_t* O, cudaStream_t s);
+
+// The same prefill attention on the tcgen05 tensor cores (head_dim 128 only).
+bool attention_tc_supported(const Shape& sh);
+int fa_error_read_and_clear();   // as tc_error_read_and_clear, for the attention kernel
+cudaError_t launch_attention_prefill_tc(const bf16_t* Q, int T, const Shape& sh, int pos0, const bf16_t* k_cache,
+                                        const bf16_t* v_cache, bf16_t* O, cudaStream_t s);
 
 // Decode attention, split over the KV length L = *pos + 1.
 // q fp32 [HQ, D]; partials sized [HQ][n_split] (+ D for o); out fp32 [HQ, D].

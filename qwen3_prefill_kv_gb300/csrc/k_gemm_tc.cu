@@ -1,0 +1,322 @@
+// Prefill GEMM on the 5th-generation tensor cores: C[M, N] (op)= A[M, K] . W[N, K]^T with bf16
+// operands (both K-major), fp32 accumulation in TMEM, and the decoder's epilogues ("Forward
+// map - funasr_nano", LLM decoder table: packed QKV projection, o_proj / down_proj with the
+// residual add, packed gate_up with SwiGLU).
+//
+// One CTA computes one 128 x BN tile with six warps:
+//   warp 0   TMA producer: 2-D tensor-map loads (128-byte swizzle) of the A tile (128 rows x
+//            64 k) and the B tile (BN rows x 64 k; SwiGLU: 64 gate rows + the 64 matching up
+//            rows) into a ring of STAGES shared-memory stages;
+//   warp 1   allocates BN TMEM columns and issues tcgen05.mma (M = 128, N = BN, K = 16) from
+//            one thread, committing each stage back to its empty barrier;
+//   warps 2-5 epilogue: tcgen05.ld of the accumulator (one TMEM lane = one output row),
+//            then store / residual add / SwiGLU to global memory.
+// Rows past M are zero-filled by TMA and never stored.  Every wait is bounded; a timeout sets
+// the error word and the CTA finishes without waiting further (TMEM is freed only after the
+// accumulator barrier).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+
+namespace qdec {
+
+__device__ int g_tc_error;   // first timeout code of a tensor-core kernel (0 = none)
+
+namespace {
+
+constexpr int BM = 128, BK = 64;
+constexpr uint32_t TC_SPIN = 1u << 22;
+
+__device__ __forceinline__ uint32_t s32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void mb_init(uint64_t* b, uint32_t c) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(s32(b)), "r"(c) : "memory");
+}
+__device__ __forceinline__ void mb_expect(uint64_t* b, uint32_t n) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(s32(b)), "r"(n) : "memory");
+}
+__device__ __forceinline__ bool mb_try(uint64_t* b, uint32_t ph) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(s32(b)), "r"(ph)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mb_wait(uint64_t* b, uint32_t ph, int code) {
+    for (uint32_t i = 0; i < TC_SPIN; ++i)
+        if (mb_try(b, ph)) return true;
+    atomicCAS(&g_tc_error, 0, code);
+    return false;
+}
+__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            s32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(s32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(s32(slot)), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(accum)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(s32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with 128-byte swizzle:
+// rows of 64 bf16 (128 B), 8-row groups 1024 B apart (stride byte offset), version 1.
+__device__ __forceinline__ uint64_t sw128_desc(const void* p) {
+    uint64_t d = (uint64_t)((s32(p) >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;              // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset
+    d |= (uint64_t)1 << 46;              // descriptor version
+    d |= (uint64_t)2 << 61;              // 128-byte swizzle
+    return d;
+}
+// Instruction descriptor: D fp32, A and B bf16, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+template <int BN, int MODE, int STAGES>
+__global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                                                         const __grid_constant__ CUtensorMap tmB, int M, int K,
+                                                         int up_off, float* __restrict__ Cf,
+                                                         bf16_t* __restrict__ Cb, int ldc) {
+    extern __shared__ __align__(1024) char smem_raw[];
+    char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    constexpr int A_BYTES = BM * BK * 2;
+    constexpr int B_BYTES = BN * BK * 2;
+    constexpr bool GLU = (MODE == GEMM_SWIGLU_BF16);
+    char* sA = smem;
+    char* sB = smem + STAGES * A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+    uint64_t* empty = full + STAGES;
+    uint64_t* accb = empty + STAGES;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(accb + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.y * BM;
+    const int n0 = blockIdx.x * (GLU ? BN / 2 : BN);   // first output column of the tile
+    const int nk = K / BK;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mb_init(&full[i], 1);
+            mb_init(&empty[i], 1);
+        }
+        mb_init(accb, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) tmem_alloc(tslot, BN);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0) {
+        if (lane == 0) {   // ---- TMA producer
+            int issued = 0;
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % STAGES, r = kb / STAGES;
+                if (!mb_wait(&empty[s], (r & 1) ^ 1, 1)) break;
+                mb_expect(&full[s], A_BYTES + B_BYTES);
+                tma_2d(sA + s * A_BYTES, &tmA, kb * BK, m0, &full[s]);
+                if (GLU) {
+                    tma_2d(sB + s * B_BYTES, &tmB, kb * BK, n0, &full[s]);
+                    tma_2d(sB + s * B_BYTES + (BN / 2) * 128, &tmB, kb * BK, up_off + n0, &full[s]);
+                } else {
+                    tma_2d(sB + s * B_BYTES, &tmB, kb * BK, n0, &full[s]);
+                }
+                issued = kb + 1;
+            }
+            // copies the MMA warp did not consume (only after an error) must land before exit
+            for (int kb = issued - STAGES > 0 ? issued - STAGES : 0; kb < issued; ++kb)
+                mb_wait(&full[kb % STAGES], (kb / STAGES) & 1, 4);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {   // ---- MMA issuer
+            constexpr uint32_t idesc = idesc_bf16(BM, BN);
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % STAGES, r = kb / STAGES;
+                if (!mb_wait(&full[s], r & 1, 2)) break;
+                tc_fence_after();
+                const uint64_t ad = sw128_desc(sA + s * A_BYTES), bd = sw128_desc(sB + s * B_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)   // 16 bf16 = 32 B per MMA: +2 in the address field
+                    mma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                mma_commit(&empty[s]);
+            }
+            mma_commit(accb);   // arrives once every MMA issued above has completed
+        }
+    } else {   // ---- epilogue: warps 2..5 cover TMEM lane quarters 2, 3, 0, 1
+        mb_wait(accb, 0, 3);
+        tc_fence_after();
+        const int q = warp & 3;
+        const int row = m0 + 32 * q + lane;
+        const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
+        if (GLU) {
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+                float g[32], u[32];
+                tmem_ld32(taddr + c0, g);
+                tmem_ld32(taddr + BN / 2 + c0, u);
+                if (row < M) {
+                    uint4* dst = reinterpret_cast<uint4*>(Cb + (size_t)row * ldc + n0 + c0);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint4 w;
+                        w.x = pack_bf2(silu(g[8 * j + 0]) * u[8 * j + 0], silu(g[8 * j + 1]) * u[8 * j + 1]);
+                        w.y = pack_bf2(silu(g[8 * j + 2]) * u[8 * j + 2], silu(g[8 * j + 3]) * u[8 * j + 3]);
+                        w.z = pack_bf2(silu(g[8 * j + 4]) * u[8 * j + 4], silu(g[8 * j + 5]) * u[8 * j + 5]);
+                        w.w = pack_bf2(silu(g[8 * j + 6]) * u[8 * j + 6], silu(g[8 * j + 7]) * u[8 * j + 7]);
+                        dst[j] = w;
+                    }
+                }
+            }
+        } else {
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                float v[32];
+                tmem_ld32(taddr + c0, v);
+                if (row < M) {
+                    if (MODE == GEMM_STORE_BF16) {
+                        uint4* dst = reinterpret_cast<uint4*>(Cb + (size_t)row * ldc + n0 + c0);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            dst[j] = make_uint4(pack_bf2(v[8 * j], v[8 * j + 1]), pack_bf2(v[8 * j + 2], v[8 * j + 3]),
+                                                pack_bf2(v[8 * j + 4], v[8 * j + 5]), pack_bf2(v[8 * j + 6], v[8 * j + 7]));
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(Cf + (size_t)row * ldc + n0 + c0);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            float4 o = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                            if (MODE == GEMM_ADD_F32) {
+                                const float4 c = dst[j];
+                                o.x += c.x; o.y += c.y; o.z += c.z; o.w += c.w;
+                            }
+                            dst[j] = o;
+                        }
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, BN);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+// 2-D bf16 map of a row-major [rows, cols] matrix (row stride in elements), box 64 x box_rows.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint64_t stride_elems,
+              uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {stride_elems * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, int MODE, int STAGES>
+cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N, int K, int up_off, float* Cf,
+                      bf16_t* Cb, int ldc, cudaStream_t s) {
+    constexpr int smem = STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 256;
+    auto kern = gemm_tc_kernel<BN, MODE, STAGES>;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int tile_n = (MODE == GEMM_SWIGLU_BF16) ? BN / 2 : BN;
+    dim3 grid(N / tile_n, (M + BM - 1) / BM);
+    kern<<<grid, 192, smem, s>>>(ma, mb, M, K, up_off, Cf, Cb, ldc);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool gemm_tc_supported(int N, int K, int mode, int lda) {
+    if (K % BK != 0 || lda % 8 != 0) return false;
+    if (mode == GEMM_SWIGLU_BF16) return N % 64 == 0;
+    return N % 128 == 0;
+}
+
+cudaError_t launch_gemm_tc(const bf16_t* A, int lda, const bf16_t* W, int M, int N, int K, int mode, int up_off,
+                           float* Cf, bf16_t* Cb, int ldc, cudaStream_t s) {
+    (void)cudaGetLastError();
+    if (!gemm_tc_supported(N, K, mode, lda) || M <= 0) return cudaErrorInvalidValue;
+    CUtensorMap ma, mb;
+    const int w_rows = (mode == GEMM_SWIGLU_BF16) ? up_off + N : N;
+    if (!make_map(&ma, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, BM)) return cudaErrorInvalidValue;
+    if (!make_map(&mb, W, (uint64_t)w_rows, (uint64_t)K, (uint64_t)K, mode == GEMM_SWIGLU_BF16 ? 64 : 128))
+        return cudaErrorInvalidValue;
+    switch (mode) {
+        case GEMM_STORE_F32: return launch_bn<128, GEMM_STORE_F32, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, s);
+        case GEMM_ADD_F32: return launch_bn<128, GEMM_ADD_F32, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, s);
+        case GEMM_SWIGLU_BF16: return launch_bn<128, GEMM_SWIGLU_BF16, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, s);
+        case GEMM_STORE_BF16: return launch_bn<128, GEMM_STORE_BF16, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+int tc_error_read_and_clear() {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_tc_error, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    if (v) {
+        const int z = 0;
+        cudaMemcpyToSymbol(g_tc_error, &z, sizeof(int));
+    }
+    return v;
+}
+
+}  // namespace qdec

@@ -27,7 +27,20 @@ int qdec_op_gemm(const void* A, int32_t lda, const void* W, int32_t M, int32_t N
         return cuda_status(launch_gemm_simt(static_cast<const bf16_t*>(A), lda, static_cast<const bf16_t*>(W), M, N,
                                             K, mode, up_off, Cf, Cb, ldc, s));
     }
-    return QDEC_E_UNSUPPORTED;
+    if (impl == QDEC_IMPL_TCGEN05) {
+        if (!gemm_tc_supported(N, K, mode, lda))
+            return set_error(QDEC_E_UNSUPPORTED, "tcgen05 GEMM needs K %% 64 == 0, N %% 128 == 0 (SwiGLU: %% 64)");
+        return cuda_status(launch_gemm_tc(static_cast<const bf16_t*>(A), lda, static_cast<const bf16_t*>(W), M, N, K,
+                                          mode, up_off, Cf, Cb, ldc, s));
+    }
+    return set_error(QDEC_E_INVALID_ARG, "unknown impl %d", impl);
+}
+
+int qdec_op_device_error(void) {
+    const int v1 = tc_error_read_and_clear(), v2 = fa_error_read_and_clear();
+    if (v1 < 0 || v2 < 0) return set_error(QDEC_E_CUDA, "reading the device error word failed");
+    const int v = v1 ? v1 : v2;
+    return v ? set_error(QDEC_E_TIMEOUT, "a tensor-core kernel gave up waiting (code %d)", v) : QDEC_OK;
 }
 
 int qdec_op_attention_prefill(const void* Q, int32_t T, int32_t HQ, int32_t HKV, int32_t D, int32_t max_seq,
@@ -46,7 +59,13 @@ int qdec_op_attention_prefill(const void* Q, int32_t T, int32_t HQ, int32_t HKV,
         return cuda_status(launch_attention_prefill_simt(static_cast<const bf16_t*>(Q), T, sh, pos0,
                                                          static_cast<const bf16_t*>(k_cache),
                                                          static_cast<const bf16_t*>(v_cache), static_cast<bf16_t*>(O), s));
-    return QDEC_E_UNSUPPORTED;
+    if (impl == QDEC_IMPL_TCGEN05) {
+        if (!attention_tc_supported(sh)) return set_error(QDEC_E_UNSUPPORTED, "tcgen05 attention needs head_dim 128");
+        return cuda_status(launch_attention_prefill_tc(static_cast<const bf16_t*>(Q), T, sh, pos0,
+                                                       static_cast<const bf16_t*>(k_cache),
+                                                       static_cast<const bf16_t*>(v_cache), static_cast<bf16_t*>(O), s));
+    }
+    return set_error(QDEC_E_INVALID_ARG, "unknown impl %d", impl);
 }
 
 size_t qdec_op_lm_head_scratch_bytes(int32_t V) { return V > 0 ? lm_head_scratch_bytes(V) : 0; }

@@ -27,7 +27,7 @@ GEMM_CASES = [(1, 256, 128), (37, 256, 128), (130, 384, 384), (77, 4096, 1024), 
               (415, 1024, 3072)]
 
 
-@pytest.mark.parametrize("impl", [_lib.IMPL_SIMT])
+@pytest.mark.parametrize("impl", [_lib.IMPL_SIMT, _lib.IMPL_TCGEN05], ids=["simt", "tcgen05"])
 @pytest.mark.parametrize("M,N,K", GEMM_CASES)
 @pytest.mark.parametrize("mode", [_lib.GEMM_STORE_F32, _lib.GEMM_ADD_F32, _lib.GEMM_SWIGLU_BF16, _lib.GEMM_STORE_BF16])
 def test_gemm_epilogues(impl, M, N, K, mode):
@@ -47,15 +47,19 @@ def test_gemm_epilogues(impl, M, N, K, mode):
         got = Cd.cpu().double()
         tol = 8e-3 * ref.abs().max().item()
     torch.cuda.synchronize()
+    _lib.device_error()
     assert (got - ref).abs().max().item() <= tol
 
 
-ATTN_CASES = [(77, 4, 2, 32, 0), (64, 16, 8, 128, 0), (200, 16, 8, 128, 0), (33, 4, 2, 32, 40), (5, 16, 8, 128, 100)]
+ATTN_CASES = [(77, 4, 2, 32, 0), (64, 16, 8, 128, 0), (200, 16, 8, 128, 0), (33, 4, 2, 32, 40), (5, 16, 8, 128, 100),
+              (415, 16, 8, 128, 0), (1000, 16, 8, 128, 0), (130, 4, 4, 128, 0), (300, 8, 1, 128, 0)]
 
 
-@pytest.mark.parametrize("impl", [_lib.IMPL_SIMT])
+@pytest.mark.parametrize("impl", [_lib.IMPL_SIMT, _lib.IMPL_TCGEN05], ids=["simt", "tcgen05"])
 @pytest.mark.parametrize("T,HQ,HKV,D,pos0", ATTN_CASES)
 def test_attention_prefill(impl, T, HQ, HKV, D, pos0):
+    if impl == _lib.IMPL_TCGEN05 and D != 128:
+        pytest.skip("the tensor-core attention covers head_dim 128")
     L = pos0 + T
     max_seq = L + 7
     Q = _bf16((T, HQ, D), 3)
@@ -64,6 +68,7 @@ def test_attention_prefill(impl, T, HQ, HKV, D, pos0):
     O = torch.zeros(T, HQ * D, dtype=torch.bfloat16, device="cuda")
     _lib.attention_prefill(Q.cuda(), T, HQ, HKV, D, max_seq, pos0, K.cuda(), Vv.cuda(), O, impl=impl)
     torch.cuda.synchronize()
+    _lib.device_error()
     ref = oracle.causal_gqa_attention(Q.double().numpy(), K[:, :L].permute(1, 0, 2).double().numpy(),
                                       Vv[:, :L].permute(1, 0, 2).double().numpy(),
                                       np.arange(pos0, pos0 + T), np.arange(L)).reshape(T, HQ * D)
