@@ -19,6 +19,7 @@ extern "C" {
 #define QDEC_GEMM_ADD_F32     1   /* C[m,n] += acc   (residual add)             (fp32 C) */
 #define QDEC_GEMM_SWIGLU_BF16 2   /* C[m,n] = silu(gate) * up, W = [gate rows; up rows at up_off] (bf16 C) */
 #define QDEC_GEMM_STORE_BF16  3   /* C[m,n] = bf16(acc)                         (bf16 C) */
+#define QDEC_GEMM_ATOMIC_F32  4   /* C[m,n] += acc with fp32 atomics (TCGEN05 only; fp32 C) */
 
 #define QDEC_IMPL_SIMT     0      /* CUDA-core kernel */
 #define QDEC_IMPL_TCGEN05  1      /* tcgen05 / TMEM / TMA kernel */
@@ -30,6 +31,14 @@ extern "C" {
  * elements.  Shape limits: K % 64 == 0 for TCGEN05, K % 32 == 0 for SIMT. */
 int qdec_op_gemm(const void *A, int32_t lda, const void *W, int32_t M, int32_t N, int32_t K, int32_t mode,
                  int32_t up_off, void *C, int32_t ldc, int32_t impl, void *stream);
+
+/* C[M, N] += A[M, K] . W[N, K]^T on the tcgen05 tensor cores with K split over
+ * `splits` CTAs per output tile whose fp32 partials are added with atomics
+ * (summation order, hence the last bits, may vary between runs).  Used by the
+ * few-row GEMMs of the lockstep batch decode.  Shape limits as TCGEN05 above;
+ * C fp32 with row stride ldc (16-byte aligned rows). */
+int qdec_op_gemm_splitk(const void *A, int32_t lda, const void *W, int32_t M, int32_t N, int32_t K, int32_t splits,
+                        float *C, int32_t ldc, void *stream);
 
 /* Synchronises the device and reports whether a tensor-core kernel launched
  * through these entry points gave up on a bounded wait since the last call:

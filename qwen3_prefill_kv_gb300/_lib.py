@@ -19,7 +19,7 @@ QDEC_OK = 0
 STATUS = {-1: "INVALID_ARG", -2: "CAPACITY", -3: "STATE", -4: "CUDA", -5: "OOM", -6: "TIMEOUT",
           -7: "UNSUPPORTED"}
 
-GEMM_STORE_F32, GEMM_ADD_F32, GEMM_SWIGLU_BF16, GEMM_STORE_BF16 = 0, 1, 2, 3
+GEMM_STORE_F32, GEMM_ADD_F32, GEMM_SWIGLU_BF16, GEMM_STORE_BF16, GEMM_ATOMIC_F32 = 0, 1, 2, 3, 4
 OPT_DECODE_KERNEL = 1
 OPT_TRACE = 2
 OPT_PREFILL_IMPL = 3
@@ -72,6 +72,7 @@ SIGNATURES = [
     ("qdec_kernel_launches", C.c_uint64, []),
     ("qdec_op_gemm", C.c_int, [_VP, _I32, _VP, _I32, _I32, _I32, _I32, _I32, _VP, _I32, _I32, _VP]),
     ("qdec_op_device_error", C.c_int, []),
+    ("qdec_op_gemm_splitk", C.c_int, [_VP, _I32, _VP, _I32, _I32, _I32, _I32, _VP, _I32, _VP]),
     ("qdec_op_attention_prefill", C.c_int, [_VP, _I32, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _I32, _VP]),
     ("qdec_op_lm_head_scratch_bytes", _SZ, [_I32]),
     ("qdec_op_lm_head_argmax", C.c_int, [_VP, _I32, _I32, _VP, _VP, _F, _VP, _VP, _VP, _SZ, _VP]),
@@ -249,6 +250,13 @@ def gemm(A, W, M, N, K, mode, C_out, lda=None, ldc=None, up_off=0, impl=IMPL_SIM
     lib = load()
     _check(lib.qdec_op_gemm(_ptr(A), lda if lda is not None else K, _ptr(W), M, N, K, mode, up_off, _ptr(C_out),
                             ldc if ldc is not None else N, impl, _stream_handle(stream)))
+
+
+def gemm_splitk(A, W, M, N, K, splits, C_out, lda=None, ldc=None, stream=None) -> None:
+    """C += A . W^T on the tensor cores with K split over `splits` CTAs (fp32 atomics)."""
+    lib = load()
+    _check(lib.qdec_op_gemm_splitk(_ptr(A), lda if lda is not None else K, _ptr(W), M, N, K, splits, _ptr(C_out),
+                                   ldc if ldc is not None else N, _stream_handle(stream)))
 
 
 def device_error() -> None:

@@ -75,6 +75,27 @@ static unsigned long long g_launches = 0;
 void count_launches(uint64_t n) { __atomic_fetch_add(&g_launches, (unsigned long long)n, __ATOMIC_RELAXED); }
 }  // namespace qdec
 
+// Workspace of a lockstep batch step (owned by the batch's first context).
+struct BatchWork {
+    int cap = 0;                         // streams the buffers hold
+    std::vector<const qdec_ctx*> members;   // composition the stream table was built for
+    BatchStream* d_streams = nullptr;
+    int* d_tokens = nullptr;
+    int* d_am = nullptr;
+    int* h_am = nullptr;                 // pinned
+    float *X = nullptr, *qkv = nullptr, *q = nullptr, *part_ml = nullptr, *part_o = nullptr, *gu = nullptr,
+          *logits = nullptr;
+    bf16_t *Xn = nullptr, *attn = nullptr, *h = nullptr;
+    int n_split = 1;
+    void release() {
+        void* ps[] = {d_streams, d_tokens, d_am, X, qkv, q, part_ml, part_o, gu, logits, Xn, attn, h};
+        for (void* p : ps)
+            if (p) cudaFree(p);
+        if (h_am) cudaFreeHost(h_am);
+        *this = BatchWork();
+    }
+};
+
 struct qdec_ctx {
     qdec_config cfg;
     Shape sh;
@@ -131,6 +152,8 @@ struct qdec_ctx {
     int* d_err = nullptr;                // d_argmax + 1
     unsigned long long* d_trace = nullptr;   // phase trace of the persistent step (QDEC_OPT_TRACE)
     int prefill_gemm = QDEC_PREFILL_TCGEN05;
+    BatchWork* batch = nullptr;          // lockstep-batch workspace when this context led a batch
+    int sms = 0;
 
     size_t kv_layer_stride() const { return (size_t)2 * sh.HKV * sh.max_seq * sh.D; }
     bf16_t* k_cache(int l) { return kv + (size_t)l * kv_layer_stride(); }
@@ -145,6 +168,11 @@ cudaError_t dalloc(T** p, size_t n) {
 }
 
 void free_all(qdec_ctx* c) {
+    if (c->batch) {
+        c->batch->release();
+        delete c->batch;
+        c->batch = nullptr;
+    }
     if (c->decode_exec) cudaGraphExecDestroy(c->decode_exec);
     void* ptrs[] = {c->kv, c->rope, c->d_hist, c->d_pos, c->d_zero, c->d_argmax, c->d_x, c->d_qkv, c->d_q,
                     c->d_attn, c->d_h, c->d_logits, c->d_part_ml, c->d_part_o, c->d_lm_scratch, c->p_X,
@@ -185,6 +213,7 @@ int alloc_persistent(qdec_ctx* c);
 int alloc_state(qdec_ctx* c) {
     const Shape& sh = c->sh;
     CK(cudaGetDevice(&c->device));
+    CK(cudaDeviceGetAttribute(&c->sms, cudaDevAttrMultiProcessorCount, c->device));
     CK(cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking));
     CK(dalloc(&c->kv, (size_t)sh.NL * c->kv_layer_stride()));
     CK(cudaMemset(c->kv, 0, (size_t)sh.NL * c->kv_layer_stride() * sizeof(bf16_t)));
@@ -466,6 +495,126 @@ int check_decode_args(const qdec_ctx* c, int token) {
     return QDEC_OK;
 }
 
+// ---------------------------------------------------------------- lockstep batch
+int ensure_batch_work(qdec_ctx* const* ctxs, int n) {
+    qdec_ctx* c0 = ctxs[0];
+    const Shape& sh = c0->sh;
+    if (!c0->batch) c0->batch = new (std::nothrow) BatchWork();
+    if (!c0->batch) return fail(QDEC_E_OOM, "host allocation failed");
+    BatchWork& b = *c0->batch;
+    if (n > b.cap) {
+        CK(cudaStreamSynchronize(c0->stream));
+        b.release();
+        const int target = 4 * c0->sms;
+        int ns = (target + sh.HKV * n - 1) / (sh.HKV * n);
+        b.n_split = ns < 1 ? 1 : (ns > 32 ? 32 : ns);
+        const size_t qd = (size_t)sh.HQ * sh.D;
+        CK(dalloc(&b.d_streams, (size_t)n));
+        CK(dalloc(&b.d_tokens, (size_t)n));
+        CK(dalloc(&b.d_am, (size_t)n));
+        CK(cudaMallocHost(reinterpret_cast<void**>(&b.h_am), (size_t)n * sizeof(int)));
+        CK(dalloc(&b.X, (size_t)n * sh.H));
+        CK(dalloc(&b.Xn, (size_t)n * sh.H));
+        CK(dalloc(&b.qkv, (size_t)n * sh.qkv_rows()));
+        CK(dalloc(&b.q, (size_t)n * qd));
+        CK(dalloc(&b.part_ml, (size_t)n * sh.HQ * b.n_split * 2));
+        CK(dalloc(&b.part_o, (size_t)n * sh.HQ * b.n_split * sh.D));
+        CK(dalloc(&b.attn, (size_t)n * qd));
+        CK(dalloc(&b.gu, (size_t)n * 2 * sh.F));
+        CK(dalloc(&b.h, (size_t)n * sh.F));
+        CK(dalloc(&b.logits, (size_t)n * sh.V));
+        b.cap = n;
+    }
+    bool same = (int)b.members.size() == n;
+    for (int i = 0; same && i < n; ++i) same = b.members[i] == ctxs[i];
+    if (!same) {
+        std::vector<BatchStream> hs(n);
+        b.members.assign(ctxs, ctxs + n);
+        for (int i = 0; i < n; ++i)
+            hs[i] = BatchStream{ctxs[i]->kv, ctxs[i]->d_pos, ctxs[i]->d_argmax, ctxs[i]->d_hist, ctxs[i]->rope,
+                                ctxs[i]->sh.max_seq};
+        CK(cudaMemcpyAsync(b.d_streams, hs.data(), n * sizeof(BatchStream), cudaMemcpyHostToDevice, c0->stream));
+        CK(cudaStreamSynchronize(c0->stream));   // hs is pageable host memory that goes out of scope
+    }
+    return QDEC_OK;
+}
+
+// C[n, N] = A . W^T, stored (accumulate = false) or added into C: tcgen05 with split-K fp32
+// atomics where the shape allows it (the few-row batch GEMM needs the extra CTAs), CUDA cores
+// otherwise.
+int batch_gemm(qdec_ctx* c, const bf16_t* A, int lda, const bf16_t* W, int M, int N, int K, bool accumulate,
+               float* C, int ldc, cudaStream_t s) {
+    if (c->prefill_gemm == QDEC_PREFILL_TCGEN05 && gemm_tc_supported(N, K, GEMM_ATOMIC_F32, lda)) {
+        if (!accumulate) CK(cudaMemsetAsync(C, 0, (size_t)M * ldc * sizeof(float), s));
+        const int tiles = (N / 128) * ((M + 127) / 128);
+        const int splits = (2 * c->sms + tiles - 1) / tiles;
+        CK(launch_gemm_tc(A, lda, W, M, N, K, GEMM_ATOMIC_F32, 0, C, nullptr, ldc, s, splits));
+        return QDEC_OK;
+    }
+    CK(launch_gemm_simt(A, lda, W, M, N, K, accumulate ? GEMM_ADD_F32 : GEMM_STORE_F32, 0, C, nullptr, ldc, s));
+    return QDEC_OK;
+}
+
+int batch_step(qdec_ctx* const* ctxs, int n, const int32_t* tokens, float* logits_out, int32_t* argmax_out) {
+    qdec_ctx* c0 = ctxs[0];
+    const Shape& sh = c0->sh;
+    cudaStream_t s = c0->stream;
+    // order against work queued on the other contexts' streams
+    std::vector<cudaEvent_t> evs;
+    for (int i = 1; i < n; ++i) {
+        if (ctxs[i]->stream == s) continue;
+        cudaEvent_t e;
+        CK(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+        evs.push_back(e);
+        CK(cudaEventRecord(e, ctxs[i]->stream));
+        CK(cudaStreamWaitEvent(s, e, 0));
+    }
+    int rc = ensure_batch_work(ctxs, n);
+    if (rc != QDEC_OK) return rc;
+    BatchWork& b = *c0->batch;
+    CK(cudaMemcpyAsync(b.d_tokens, tokens, (size_t)n * sizeof(int), cudaMemcpyHostToDevice, s));
+    CK(launch_batch_embed(c0->embed, sh.H, b.d_tokens, b.d_streams, n, b.X, s));
+    const int qd = sh.HQ * sh.D;
+    uint64_t kernels = 1;
+    for (int l = 0; l < sh.NL; ++l) {
+        const LayerW& w = c0->layers[l];
+        CK(launch_rmsnorm_bf16(b.X, n, sh.H, w.g_in, sh.eps, b.Xn, s));
+        if ((rc = batch_gemm(c0, b.Xn, sh.H, w.wqkv, n, sh.qkv_rows(), sh.H, false, b.qkv, sh.qkv_rows(), s))) return rc;
+        CK(launch_batch_qk_rope(b.qkv, sh, l, w.g_q, w.g_k, b.d_streams, n, b.q, s));
+        CK(launch_batch_attention(b.q, sh, l, b.d_streams, n, b.n_split, b.part_ml, b.part_o, b.attn, s));
+        if ((rc = batch_gemm(c0, b.attn, qd, w.wo, n, sh.H, qd, true, b.X, sh.H, s))) return rc;
+        CK(launch_rmsnorm_bf16(b.X, n, sh.H, w.g_post, sh.eps, b.Xn, s));
+        if ((rc = batch_gemm(c0, b.Xn, sh.H, w.wgu, n, 2 * sh.F, sh.H, false, b.gu, 2 * sh.F, s))) return rc;
+        CK(launch_batch_swiglu(b.gu, sh.F, n, b.h, s));
+        if ((rc = batch_gemm(c0, b.h, sh.F, w.wd, n, sh.H, sh.F, true, b.X, sh.H, s))) return rc;
+        kernels += 12;
+    }
+    CK(launch_rmsnorm_bf16(b.X, n, sh.H, c0->final_norm, sh.eps, b.Xn, s));
+    float* lg = (logits_out && is_device_ptr(logits_out) && aligned16(logits_out)) ? logits_out : b.logits;
+    if ((rc = batch_gemm(c0, b.Xn, sh.H, c0->embed, n, sh.V, sh.H, false, lg, sh.V, s))) return rc;
+    CK(launch_batch_argmax(lg, sh.V, sh.V, b.d_streams, n, b.d_am, s));
+    count_launches(kernels + 3);
+    for (int i = 0; i < n; ++i) ctxs[i]->position += 1;
+    if (logits_out && lg != logits_out)
+        CK(cudaMemcpyAsync(logits_out, lg, (size_t)n * sh.V * sizeof(float), cudaMemcpyDefault, s));
+    for (cudaEvent_t e : evs) {   // the other streams wait for the batch before their next work
+        CK(cudaEventRecord(e, s));
+    }
+    int k = 0;
+    for (int i = 1; i < n; ++i) {
+        if (ctxs[i]->stream == s) continue;
+        CK(cudaStreamWaitEvent(ctxs[i]->stream, evs[k++], 0));
+    }
+    for (cudaEvent_t e : evs) cudaEventDestroy(e);
+    if (argmax_out) {
+        CK(cudaMemcpyAsync(b.h_am, b.d_am, (size_t)n * sizeof(int), cudaMemcpyDeviceToHost, s));
+        rc = sync_status(c0, 6, nullptr);
+        if (rc != QDEC_OK) return rc;
+        for (int i = 0; i < n; ++i) argmax_out[i] = b.h_am[i];
+    }
+    return QDEC_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -589,26 +738,14 @@ int qdec_decode_step_batch(qdec_ctx* const* ctxs, int32_t n, const int32_t* toke
     for (int i = 0; i < n; ++i) {
         int rc = check_decode_args(ctxs[i], tokens[i]);
         if (rc != QDEC_OK) return rc;
-        if (ctxs[i]->embed != ctxs[0]->embed || memcmp(&ctxs[i]->cfg, &ctxs[0]->cfg, sizeof(qdec_config)) != 0)
-            return fail(QDEC_E_STATE, "batch contexts differ in weights or shape");
+        if (ctxs[i]->embed != ctxs[0]->embed || memcmp(&ctxs[i]->cfg, &ctxs[0]->cfg, sizeof(qdec_config)) != 0 ||
+            ctxs[i]->device != ctxs[0]->device)
+            return fail(QDEC_E_STATE, "batch contexts differ in weights, shape or device");
         for (int j = 0; j < i; ++j)
             if (ctxs[j] == ctxs[i]) return fail(QDEC_E_INVALID_ARG, "context %d repeated in the batch", i);
     }
-    const int V = ctxs[0]->sh.V;
-    for (int i = 0; i < n; ++i) {
-        qdec_ctx* c = ctxs[i];
-        int rc = enqueue_decode_step(c, tokens[i]);
-        if (rc != QDEC_OK) return rc;
-        c->position += 1;
-        if (logits_out) CK(cudaMemcpyAsync(logits_out + (size_t)i * V, c->d_logits, (size_t)V * sizeof(float),
-                                           cudaMemcpyDefault, c->stream));
-        if (argmax_out) {
-            rc = sync_status(c, 2, &argmax_out[i]);
-            if (rc != QDEC_OK) return rc;
-        }
-    }
-    for (int i = 0; i < n; ++i) CK(cudaStreamSynchronize(ctxs[i]->stream));
-    return QDEC_OK;
+    if (n == 1) return qdec_decode_step(ctxs[0], tokens[0], logits_out, argmax_out);
+    return batch_step(ctxs, n, tokens, logits_out, argmax_out);
 }
 
 int qdec_clone(const qdec_ctx* src, qdec_ctx** out) {

@@ -65,7 +65,7 @@ int set_error(int code, const char* fmt, ...);
 cudaError_t launch_rmsnorm_bf16(const float* X, int T, int H, const bf16_t* g, float eps,
                                 bf16_t* out, cudaStream_t s);
 
-enum GemmMode { GEMM_STORE_F32 = 0, GEMM_ADD_F32 = 1, GEMM_SWIGLU_BF16 = 2, GEMM_STORE_BF16 = 3 };
+enum GemmMode { GEMM_STORE_F32 = 0, GEMM_ADD_F32 = 1, GEMM_SWIGLU_BF16 = 2, GEMM_STORE_BF16 = 3, GEMM_ATOMIC_F32 = 4 };
 // C[M, N] (op) A[M, K] . W[N, K]^T.  SWIGLU: W is [2N, K] (gate rows, then up rows at
 // offset `up_off` rows) and C_bf16[m, n] = silu(gate) * up.
 cudaError_t launch_gemm_simt(const bf16_t* A, int lda, const bf16_t* W, int M, int N, int K, int mode,
@@ -74,8 +74,9 @@ cudaError_t launch_gemm_simt(const bf16_t* A, int lda, const bf16_t* W, int M, i
 // The same GEMM on the tcgen05 tensor cores (TMA-fed, TMEM accumulator).  Needs K % 64 == 0,
 // lda % 8 == 0, N % 128 == 0 (SwiGLU: N % 64 == 0) and 16-byte aligned A, W.
 bool gemm_tc_supported(int N, int K, int mode, int lda);
+// GEMM_ATOMIC_F32 (C += acc with fp32 vector atomics) may split K over `splits` CTAs per tile.
 cudaError_t launch_gemm_tc(const bf16_t* A, int lda, const bf16_t* W, int M, int N, int K, int mode, int up_off,
-                           float* Cf, bf16_t* Cb, int ldc, cudaStream_t s);
+                           float* Cf, bf16_t* Cb, int ldc, cudaStream_t s, int splits = 1);
 // First timeout code recorded by a tensor-core kernel since the last call (0 = none);
 // synchronous, clears the flag.
 int tc_error_read_and_clear();
@@ -117,6 +118,25 @@ cudaError_t launch_gemv(const bf16_t* W, int rows, int K, const float* x, const 
 size_t lm_head_scratch_bytes(int V);
 cudaError_t launch_lm_head_argmax(const bf16_t* E, int V, int H, const float* x, const bf16_t* g_final,
                                   float eps, float* logits, int* argmax, void* scratch, cudaStream_t s);
+
+// ---------------------------------------------------------------- batched (lockstep) decode
+struct BatchStream {        // one context of a lockstep batch
+    bf16_t* kv;             // its KV cache [NL][2][HKV][max_seq][D]
+    int* pos;               // its device position (advanced by the step)
+    int* argmax;            // its previous / new argmax
+    int* hist;              // its token history
+    const float2* rope;     // its RoPE table
+    int max_seq;
+};
+cudaError_t launch_batch_embed(const bf16_t* E, int H, const int* tokens, const BatchStream* bs, int n, float* X,
+                               cudaStream_t st);
+cudaError_t launch_batch_qk_rope(const float* qkv, const Shape& sh, int layer, const bf16_t* g_q, const bf16_t* g_k,
+                                 const BatchStream* bs, int n, float* q_out, cudaStream_t st);
+cudaError_t launch_batch_attention(const float* q, const Shape& sh, int layer, const BatchStream* bs, int n, int n_split,
+                                   float* part_ml, float* part_o, bf16_t* out, cudaStream_t st);
+cudaError_t launch_batch_swiglu(const float* gu, int F, int n, bf16_t* h, cudaStream_t st);
+cudaError_t launch_batch_argmax(const float* logits, int V, int ld, const BatchStream* bs, int n, int* out,
+                                cudaStream_t st);
 
 // ---------------------------------------------------------------- persistent decode
 struct DecodeLayer {

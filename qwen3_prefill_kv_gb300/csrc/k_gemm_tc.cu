@@ -122,7 +122,10 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.y * BM;
     const int n0 = blockIdx.x * (GLU ? BN / 2 : BN);   // first output column of the tile
-    const int nk = K / BK;
+    // split-K: CTA z of gridDim.z handles k-blocks [kb0, kb0 + nk)
+    const int nkb = K / BK, per = (nkb + gridDim.z - 1) / gridDim.z;
+    const int kb0 = blockIdx.z * per;
+    const int nk = max(0, min(nkb, kb0 + per) - kb0);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
@@ -145,12 +148,12 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
                 const int s = kb % STAGES, r = kb / STAGES;
                 if (!mb_wait(&empty[s], (r & 1) ^ 1, 1)) break;
                 mb_expect(&full[s], A_BYTES + B_BYTES);
-                tma_2d(sA + s * A_BYTES, &tmA, kb * BK, m0, &full[s]);
+                tma_2d(sA + s * A_BYTES, &tmA, (kb0 + kb) * BK, m0, &full[s]);
                 if (GLU) {
-                    tma_2d(sB + s * B_BYTES, &tmB, kb * BK, n0, &full[s]);
-                    tma_2d(sB + s * B_BYTES + (BN / 2) * 128, &tmB, kb * BK, up_off + n0, &full[s]);
+                    tma_2d(sB + s * B_BYTES, &tmB, (kb0 + kb) * BK, n0, &full[s]);
+                    tma_2d(sB + s * B_BYTES + (BN / 2) * 128, &tmB, (kb0 + kb) * BK, up_off + n0, &full[s]);
                 } else {
-                    tma_2d(sB + s * B_BYTES, &tmB, kb * BK, n0, &full[s]);
+                    tma_2d(sB + s * B_BYTES, &tmB, (kb0 + kb) * BK, n0, &full[s]);
                 }
                 issued = kb + 1;
             }
@@ -171,7 +174,7 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
                     mma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
                 mma_commit(&empty[s]);
             }
-            mma_commit(accb);   // arrives once every MMA issued above has completed
+            mma_commit(accb);   // arrives once every MMA issued above has completed (nk >= 1: host)
         }
     } else {   // ---- epilogue: warps 2..5 cover TMEM lane quarters 2, 3, 0, 1
         mb_wait(accb, 0, 3);
@@ -215,6 +218,10 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             float4 o = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                            if (MODE == GEMM_ATOMIC_F32) {   // split-K partials: vector fp32 reductions
+                                atomicAdd(dst + j, o);
+                                continue;
+                            }
                             if (MODE == GEMM_ADD_F32) {
                                 const float4 c = dst[j];
                                 o.x += c.x; o.y += c.y; o.z += c.z; o.w += c.w;
@@ -265,7 +272,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 
 template <int BN, int MODE, int STAGES>
 cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N, int K, int up_off, float* Cf,
-                      bf16_t* Cb, int ldc, cudaStream_t s) {
+                      bf16_t* Cb, int ldc, int splits, cudaStream_t s) {
     constexpr int smem = STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 256;
     auto kern = gemm_tc_kernel<BN, MODE, STAGES>;
     static bool attr = false;
@@ -275,7 +282,7 @@ cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N
         attr = true;
     }
     const int tile_n = (MODE == GEMM_SWIGLU_BF16) ? BN / 2 : BN;
-    dim3 grid(N / tile_n, (M + BM - 1) / BM);
+    dim3 grid(N / tile_n, (M + BM - 1) / BM, splits);
     kern<<<grid, 192, smem, s>>>(ma, mb, M, K, up_off, Cf, Cb, ldc);
     return cudaGetLastError();
 }
@@ -289,19 +296,26 @@ bool gemm_tc_supported(int N, int K, int mode, int lda) {
 }
 
 cudaError_t launch_gemm_tc(const bf16_t* A, int lda, const bf16_t* W, int M, int N, int K, int mode, int up_off,
-                           float* Cf, bf16_t* Cb, int ldc, cudaStream_t s) {
+                           float* Cf, bf16_t* Cb, int ldc, cudaStream_t s, int splits) {
     (void)cudaGetLastError();
     if (!gemm_tc_supported(N, K, mode, lda) || M <= 0) return cudaErrorInvalidValue;
+    // each split needs at least one k-block; only the atomic mode may be split
+    const int nkb = K / BK;
+    if (splits < 1 || (splits > 1 && mode != GEMM_ATOMIC_F32)) return cudaErrorInvalidValue;
+    if (splits > nkb) splits = nkb;
+    const int per = (nkb + splits - 1) / splits;
+    splits = (nkb + per - 1) / per;
     CUtensorMap ma, mb;
     const int w_rows = (mode == GEMM_SWIGLU_BF16) ? up_off + N : N;
     if (!make_map(&ma, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, BM)) return cudaErrorInvalidValue;
     if (!make_map(&mb, W, (uint64_t)w_rows, (uint64_t)K, (uint64_t)K, mode == GEMM_SWIGLU_BF16 ? 64 : 128))
         return cudaErrorInvalidValue;
     switch (mode) {
-        case GEMM_STORE_F32: return launch_bn<128, GEMM_STORE_F32, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, s);
-        case GEMM_ADD_F32: return launch_bn<128, GEMM_ADD_F32, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, s);
-        case GEMM_SWIGLU_BF16: return launch_bn<128, GEMM_SWIGLU_BF16, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, s);
-        case GEMM_STORE_BF16: return launch_bn<128, GEMM_STORE_BF16, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, s);
+        case GEMM_STORE_F32: return launch_bn<128, GEMM_STORE_F32, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
+        case GEMM_ADD_F32: return launch_bn<128, GEMM_ADD_F32, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
+        case GEMM_SWIGLU_BF16: return launch_bn<128, GEMM_SWIGLU_BF16, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
+        case GEMM_STORE_BF16: return launch_bn<128, GEMM_STORE_BF16, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
+        case GEMM_ATOMIC_F32: return launch_bn<128, GEMM_ATOMIC_F32, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
         default: return cudaErrorInvalidValue;
     }
 }

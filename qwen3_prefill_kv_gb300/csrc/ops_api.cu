@@ -16,13 +16,14 @@ extern "C" {
 
 int qdec_op_gemm(const void* A, int32_t lda, const void* W, int32_t M, int32_t N, int32_t K, int32_t mode,
                  int32_t up_off, void* C, int32_t ldc, int32_t impl, void* stream) {
-    if (!A || !W || !C || M <= 0 || N <= 0 || K <= 0 || mode < 0 || mode > 3)
+    if (!A || !W || !C || M <= 0 || N <= 0 || K <= 0 || mode < 0 || mode > 4)
         return set_error(QDEC_E_INVALID_ARG, "qdec_op_gemm: null pointer or bad size/mode");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const bool f32 = (mode == QDEC_GEMM_STORE_F32 || mode == QDEC_GEMM_ADD_F32);
+    const bool f32 = (mode == QDEC_GEMM_STORE_F32 || mode == QDEC_GEMM_ADD_F32 || mode == QDEC_GEMM_ATOMIC_F32);
     float* Cf = f32 ? static_cast<float*>(C) : nullptr;
     bf16_t* Cb = f32 ? nullptr : static_cast<bf16_t*>(C);
     if (impl == QDEC_IMPL_SIMT) {
+        if (mode == QDEC_GEMM_ATOMIC_F32) return set_error(QDEC_E_UNSUPPORTED, "the atomic mode is tcgen05-only");
         if (K % 32 != 0 || lda % 8 != 0) return set_error(QDEC_E_UNSUPPORTED, "SIMT GEMM needs K %% 32 == 0, lda %% 8 == 0");
         return cuda_status(launch_gemm_simt(static_cast<const bf16_t*>(A), lda, static_cast<const bf16_t*>(W), M, N,
                                             K, mode, up_off, Cf, Cb, ldc, s));
@@ -34,6 +35,16 @@ int qdec_op_gemm(const void* A, int32_t lda, const void* W, int32_t M, int32_t N
                                           mode, up_off, Cf, Cb, ldc, s));
     }
     return set_error(QDEC_E_INVALID_ARG, "unknown impl %d", impl);
+}
+
+int qdec_op_gemm_splitk(const void* A, int32_t lda, const void* W, int32_t M, int32_t N, int32_t K, int32_t splits,
+                        float* C, int32_t ldc, void* stream) {
+    if (!A || !W || !C || M <= 0 || N <= 0 || K <= 0 || splits < 1)
+        return set_error(QDEC_E_INVALID_ARG, "qdec_op_gemm_splitk: null pointer or bad size");
+    if (!gemm_tc_supported(N, K, GEMM_ATOMIC_F32, lda))
+        return set_error(QDEC_E_UNSUPPORTED, "tcgen05 GEMM needs K %% 64 == 0, N %% 128 == 0");
+    return cuda_status(launch_gemm_tc(static_cast<const bf16_t*>(A), lda, static_cast<const bf16_t*>(W), M, N, K,
+                                      GEMM_ATOMIC_F32, 0, C, nullptr, ldc, static_cast<cudaStream_t>(stream), splits));
 }
 
 int qdec_op_device_error(void) {

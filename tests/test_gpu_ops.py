@@ -51,6 +51,21 @@ def test_gemm_epilogues(impl, M, N, K, mode):
     assert (got - ref).abs().max().item() <= tol
 
 
+@pytest.mark.parametrize("M,N,K,splits", [(64, 4096, 1024, 8), (64, 1024, 3072, 32), (5, 256, 128, 2),
+                                          (64, 6144, 1024, 4), (130, 1024, 2048, 3)])
+def test_gemm_splitk_atomic(M, N, K, splits):
+    A = _bf16((M, K), 11)
+    W = _bf16((N, K), 12, std=0.02)
+    C0 = torch.randn(M, N)
+    Cd = C0.cuda()
+    _lib.gemm_splitk(A.cuda(), W.cuda(), M, N, K, splits, Cd)
+    torch.cuda.synchronize()
+    _lib.device_error()
+    ref = A.double() @ W.double().T
+    got = Cd.cpu().double() - C0.double()
+    assert (got - ref).abs().max().item() <= 2e-5 * ref.abs().max().item() + 1e-6
+
+
 ATTN_CASES = [(77, 4, 2, 32, 0), (64, 16, 8, 128, 0), (200, 16, 8, 128, 0), (33, 4, 2, 32, 40), (5, 16, 8, 128, 100),
               (415, 16, 8, 128, 0), (1000, 16, 8, 128, 0), (130, 4, 4, 128, 0), (300, 8, 1, 128, 0)]
 

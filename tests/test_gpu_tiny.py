@@ -198,8 +198,10 @@ def test_batch_step_matches_single_streams(model):
             ok, m = oracle.parity_gate(lb[i].cpu().numpy(), z, H.COS_MIN, H.REL_BOUND)
             assert ok, (step, i, m)
             assert am[i] == int(torch.argmax(lb[i]))
+            # the batch runs its projections on the tensor cores with bf16 activations, a
+            # single step keeps them fp32: they agree to bf16 rounding
             np.testing.assert_allclose(lb[i].cpu().numpy(), ls.cpu().numpy(), rtol=0,
-                                       atol=1e-3 * float(ls.abs().max()))
+                                       atol=1e-2 * float(ls.abs().max()))
         toks = am                                    # greedy continuation per stream
     assert all(b.position == p.ids.numel() + 4 for b in branches)
 
