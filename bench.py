@@ -191,6 +191,17 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def batch_step_bytes(shape, Ls):
+    """Algorithmic HBM bytes of one lockstep decode step over streams whose KV lengths
+    after the append are Ls: every weight once for the whole batch, each stream's KV
+    cache read [0, L-1) and its new slot written, each stream's logits row written."""
+    H, D, F = shape.hidden, shape.head_dim, shape.ffn
+    per_layer = (shape.qkv_rows * H + H * shape.n_q_heads * D + 2 * F * H + H * F + 2 * H + 2 * D) * 2
+    weights = shape.n_layers * per_layer + shape.vocab * H * 2 + H * 2 + len(Ls) * H * 2
+    kv = sum(L * shape.kv_bytes_per_position for L in Ls)
+    return weights + kv + len(Ls) * shape.vocab * 4
+
+
 def run_ours(args):
     import torch
     rank, world, local_rank = dist_env()
@@ -211,6 +222,8 @@ def run_ours(args):
     audio_dev = prompt.audio.to(dev)
     stream = torch.cuda.Stream(device=dev)
     dec = _lib.Decoder(shape, w, max_seq=wl.max_seq, stream=stream)
+    if wl.batch > 1:
+        return run_ours_batch(args, wl, dec, prompt, audio_dev, stream, dev, rank, world, local_rank)
 
     def step_device(ev_mid=None):
         dec.prefill(ids, audio_dev, prompt.audio_offset, want_argmax=False)
@@ -315,6 +328,114 @@ def run_ours(args):
         except Exception as e:  # pragma: no cover
             line["cpu_baseline"] = {"value": None, "unit": UNIT, "cores": None, "kind": "oracle",
                                     "sample": f"failed: {e}"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    dec.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_ours_batch(args, wl, dec, prompt, audio_dev, stream, dev, rank, world, local_rank):
+    """Branching workload: one prefill, wl.batch clones of its state, each with its own
+    seeded forced first token, then wl.n_decode lockstep decode steps of the whole batch
+    (each stream's argmax fed back on the device).  value = decode tokens/s of the batch."""
+    import numpy as np
+    import torch
+    from qwen3_prefill_kv_gb300 import synth
+    from qwen3_prefill_kv_gb300._lib import Decoder
+    from qwen3_prefill_kv_gb300 import _lib
+    shape, n = wl.shape, wl.batch
+    first = synth.make_tokens(shape.vocab, n, seed=rank).numpy()
+    feedback = np.full(n, -1, dtype=np.int32)
+
+    def step(ev_mid=None):
+        dec.prefill(prompt.ids, audio_dev, prompt.audio_offset, want_argmax=False)
+        br = [dec.clone() for _ in range(n)]
+        if ev_mid is not None:
+            ev_mid.record(stream)
+        Decoder.decode_step_batch(br, first, want_argmax=False)
+        for _ in range(wl.n_decode - 1):
+            Decoder.decode_step_batch(br, feedback, want_argmax=False)
+        return br
+
+    def close(br):
+        for b in br:
+            b.close()
+
+    for _ in range(args.warmup):
+        close(step())
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    pre_ms, dec_ms = [], []
+    launches = 0
+    with ClockSampler(torch.cuda.current_device() if world == 1 else local_rank) as clk:
+        for _ in range(args.steps):
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            torch.cuda.synchronize(dev)
+            l0 = _lib.kernel_launches()
+            ev[0].record(stream)
+            br = step(ev[1])
+            ev[2].record(stream)
+            torch.cuda.synchronize(dev)
+            launches += _lib.kernel_launches() - l0
+            pre_ms.append(ev[0].elapsed_time(ev[1]))
+            dec_ms.append(ev[1].elapsed_time(ev[2]))
+            close(br)
+    clocks = clk.summary()
+
+    e2e = None
+    if not args.no_e2e:
+        ids_h = prompt.ids.clone().pin_memory()
+        audio_h = prompt.audio.clone().pin_memory()
+        logits_h = torch.empty(n, shape.vocab, dtype=torch.float32).pin_memory()
+
+        def step_host():
+            dec.prefill(ids_h, audio_h, prompt.audio_offset)
+            br = [dec.clone() for _ in range(n)]
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            toks = first
+            for j in range(wl.n_decode):
+                last = j == wl.n_decode - 1
+                toks = Decoder.decode_step_batch(br, toks, logits=logits_h if last else None)
+            torch.cuda.synchronize(dev)
+            dt = time.perf_counter() - t0
+            close(br)
+            return dt
+        for _ in range(max(1, args.warmup)):
+            step_host()
+        e_dec = [step_host() for _ in range(args.steps)]
+        h2d = prompt.ids.numel() * 4 + prompt.audio.numel() * 2 + wl.n_decode * n * 4
+        d2h = (wl.n_decode + 1) * n * 4 + n * shape.vocab * 4
+        e2e = {"value": n * wl.n_decode * len(e_dec) / sum(e_dec), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_lockstep": 1e3 * sum(e_dec) / (wl.n_decode * len(e_dec))}
+
+    dec_total_s = sum(dec_ms) / 1e3
+    pre_total_s = sum(pre_ms) / 1e3
+    tot_ms_mean = (sum(dec_ms) + sum(pre_ms)) / args.steps
+    if world > 1:
+        t = torch.tensor([dec_total_s, pre_total_s, tot_ms_mean], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dec_total_s, pre_total_s, tot_ms_mean = t.tolist()
+    value = world * n * wl.n_decode * args.steps / dec_total_s
+    hbm, _, peak_kind = peaks()
+    t_lock = dec_total_s / (wl.n_decode * args.steps)
+    bytes_per_lock = sum(batch_step_bytes(shape, [wl.n_prompt + 1 + j] * n) for j in range(wl.n_decode)) / wl.n_decode
+    achieved = bytes_per_lock / t_lock / 1e9
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": tot_ms_mean, "ms_per_lockstep": 1e3 * t_lock,
+            "ms_per_token": 1e3 * t_lock / n,
+            "prefill_and_clone_ms": 1e3 * pre_total_s / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded random-init bf16 weights of the Qwen3-0.6B shape; seeded ids, audio rows "
+                    "and forced first tokens)",
+            "config": dict(workload_desc(wl), parallelism=f"replicas{world}"),
+            "roofline": {"bound": "hbm", "kernel": "lockstep decode step (all kernels of one batch step)",
+                         "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "peak_kind": peak_kind, "traffic": None,
+                         "algorithmic_bytes_per_launch": bytes_per_lock},
+            "clocks": clocks, "gpu_launches": int(launches) * world, "e2e": e2e}
     if rank == 0:
         print(json.dumps(line), flush=True)
     dec.close()
