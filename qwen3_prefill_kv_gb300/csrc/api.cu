@@ -326,17 +326,6 @@ int ensure_audio_staging(qdec_ctx* c, int n) {
     return QDEC_OK;
 }
 
-int ensure_pinned(qdec_ctx* c, int n) {
-    if (n <= c->h_pinned_cap) return QDEC_OK;
-    CK(cudaStreamSynchronize(c->stream));
-    cudaFreeHost(c->h_pinned);
-    c->h_pinned = nullptr;
-    c->h_pinned_cap = 0;
-    CK(cudaMallocHost(reinterpret_cast<void**>(&c->h_pinned), (size_t)n * sizeof(int)));
-    c->h_pinned_cap = n;
-    return QDEC_OK;
-}
-
 // Copies the step's logits to the caller (host or device) on the context's stream.
 int copy_logits_out(qdec_ctx* c, float* dst) {
     if (!dst) return QDEC_OK;

@@ -13,12 +13,15 @@
 //    16 KB shared-memory slots with 1-D TMA bulk copies (cp.async.bulk + mbarrier
 //    complete_tx), in exactly the order the consumers use them, running ahead across
 //    phase boundaries so HBM keeps streaming while the consumers wait on data.
-//  * Warps 0..NCW-1 are consumers: GEMV rows from shared memory with the input vector
-//    in registers (fp32), attention over the streamed K/V chunk, lm_head rows + argmax.
+//  * Warps 0..NCW-1 are consumers: GEMV rows from shared memory against the input
+//    vector (fp32, also in shared memory, pre-multiplied by its RMSNorm gain), attention
+//    over the streamed K/V chunk, lm_head rows + argmax.  They walk the step's phases in
+//    one loop that is not unrolled, so each code path exists once and the kernel's hot
+//    code stays small (instruction fetch, not arithmetic, bounded the first versions).
 //  * Phases exchange vectors through global memory as 64-bit words {tag, fp32 value}
-//    written with one relaxed 64-bit store; a reader polls the words themselves until
-//    every tag equals the phase's tag, so a hand-off costs one L2 round trip and there
-//    are no grid barriers.  Each phase's writers read the whole output of the previous
+//    written with one relaxed 64-bit store; a reader polls the words themselves (several
+//    16-byte polls in flight per thread) until every tag equals the phase's tag, so a
+//    hand-off costs about one L2 round trip and there are no grid barriers.  Each phase's writers read the whole output of the previous
 //    phase before writing, which makes single-buffered tags safe.
 //  * Every wait is bounded.  On timeout a CTA sets the error word, stops issuing copies,
 //    waits (bounded) for its own copies in flight and returns; the host reports
@@ -33,7 +36,8 @@ constexpr int NCW = 7;                    // consumer warps (8 warps in all: 2 p
 constexpr int NCT = 32 * NCW;             // consumer threads
 constexpr int NT = NCT + 32;              // + one producer warp
 constexpr uint32_t SLOT = 16384;          // ring slot bytes
-constexpr int MAX_EL = (3072 + NCT - 1) / NCT;   // tagged elements per consumer thread (n <= 3072)
+constexpr int MAX_PR = (3072 / 2 + NCT - 1) / NCT;   // tagged word pairs per consumer thread (n <= 3072)
+constexpr int PB = 4;                     // polls a thread keeps in flight (registers: 4 per pair)
 constexpr uint32_t SPIN_FAST = 256;       // tagged-vector polls before backing off with nanosleep
 constexpr uint32_t SPIN_LIMIT = 1u << 21; // polls (each ~0.3-1 us) before a wait gives up: about a second
 enum { PH_QKV = 0, PH_O = 1, PH_X1 = 2, PH_H = 3, PH_X2 = 4, PH_PER_LAYER = 5 };
@@ -43,8 +47,14 @@ enum { F_ABORT = 0, F_ISSUED = 1 };
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct Layout {
-    size_t ring, full, empty, xbuf, xown, att, red, flags, total;
+    size_t ring, full, empty, xbuf, xown, att, red, kred, flags, total;
 };
+
+constexpr int KS_ROWS = 8;   // rows of one K-split block
+
+// Floats of one input-vector buffer: kmax rounded up to whole 256-column chunks (the
+// permuted layout below fills chunk positions past the vector's end).
+__host__ __device__ inline int xbuf_floats(int kmax) { return (kmax + 255) / 256 * 256; }
 
 __host__ __device__ inline Layout make_layout(int nslot, int kmax, int xown_max, int att_floats) {
     Layout L;
@@ -52,10 +62,11 @@ __host__ __device__ inline Layout make_layout(int nslot, int kmax, int xown_max,
     L.ring = o;  o += (size_t)nslot * SLOT;
     L.full = o;  o += (size_t)nslot * 8;
     L.empty = o; o += (size_t)nslot * 8;
-    o = align_up(o, 16); L.xbuf = o; o += (size_t)kmax * 2 * 4;   // double-buffered
+    o = align_up(o, 16); L.xbuf = o; o += (size_t)xbuf_floats(kmax) * 2 * 4;   // double-buffered
     o = align_up(o, 16); L.xown = o; o += (size_t)xown_max * 4;
     o = align_up(o, 16); L.att = o;  o += (size_t)att_floats * 4;
     o = align_up(o, 16); L.red = o;  o += 64 * 4;
+    o = align_up(o, 16); L.kred = o; o += 2 * NCW * KS_ROWS * 4;   // double-buffered
     L.flags = o; o += 16 * 4;
     L.total = o;
     return L;
@@ -112,10 +123,9 @@ __device__ __forceinline__ void ll_store(unsigned long long* p, uint32_t tag, fl
     const unsigned long long w = ((unsigned long long)tag << 32) | (unsigned long long)__float_as_uint(v);
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
 }
-__device__ __forceinline__ unsigned long long ll_load(const unsigned long long* p) {
-    unsigned long long w;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
-    return w;
+// Two adjacent tagged words (each 8-byte half is single-copy atomic on its own).
+__device__ __forceinline__ void ll_load2(const unsigned long long* p, unsigned long long& a, unsigned long long& b) {
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
 __device__ __forceinline__ int volatile_load(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
 
@@ -143,6 +153,21 @@ __device__ __forceinline__ float dot8(const uint4 w, const float* x) {
     a = fmaf(bf_lo(w.w), x[6], a);
     a = fmaf(bf_hi(w.w), x[7], a);
     return a;
+}
+
+// Shared-memory position of input element e in the permuted layout of a phase's input
+// vector: within each 256-column chunk, the elements lane l covers (l*8 .. l*8+7) sit at
+// l*4 .. l*4+3 and 128 + l*4 .. 128 + l*4+3, so both 16-byte loads of a warp read 512
+// contiguous bytes (no bank conflicts).  Even e and e + 1 stay adjacent.
+__device__ __forceinline__ int xperm(int e) {
+    return (e & ~255) | ((e & 4) << 5) | ((e & 248) >> 1) | (e & 3);
+}
+// The 8 input values of lane `lane` in chunk c.
+__device__ __forceinline__ void load_x8(const float* xs, int c, int lane, float (&x)[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(xs + c * 256 + lane * 4);
+    const float4 b = *reinterpret_cast<const float4*>(xs + c * 256 + 128 + lane * 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
 template <int EPL>
@@ -204,9 +229,10 @@ struct Ctx {
     float* xown;
     float* att;
     float* red;
+    float* kred;
     int* flags;
     int nslot;
-    int kmax;      // floats per xbuf buffer (xbuf holds two)
+    int kmax;      // floats per xbuf buffer (xbuf holds two), a multiple of 256
 };
 
 // Sets the CTA's abort flag and the global error word (first error wins).
@@ -241,28 +267,66 @@ __device__ inline bool wait_bar(const Ctx& S, const DecodeParams& p, uint64_t* b
     return false;
 }
 
-// All consumer threads: dst[i] = value of ll[i] once its tag equals `tag`, i < n.
-// Returns the thread's partial sum of squares through *ss.  n <= MAX_EL * NCT.
-__device__ inline bool ll_fetch(const Ctx& S, const DecodeParams& p, const unsigned long long* ll, int n,
-                                uint32_t tag, float* dst, float* ss) {
+// A tagged vector to fetch: n (even) words from src (16-byte aligned).
+struct LLSeg {
+    const unsigned long long* src;
+    int n;
+};
+
+// All consumer threads: the segments' words, concatenated, into dst once every tag equals
+// `tag` (times gain[i] when `gain` is given; the sum of squares is of the raw values),
+// at dst[i] or, with PERM, at dst[xperm(i)].  A thread owns word pairs ct, ct + NCT, ...; each poll issues all of its pending
+// 16-byte loads before it looks at any result, so one round of polls costs one L2 round
+// trip per PB pairs (not one per word).  Returns the thread's partial sum of squares through *ss.
+template <int NSEG, bool PERM = false>
+__device__ __forceinline__ bool ll_fetch(const Ctx& S, const DecodeParams& p, const LLSeg (&seg)[NSEG], uint32_t tag,
+                                float* dst, float* ss, const bf16_t* gain = nullptr) {
     const int ct = threadIdx.x;
     if (reinterpret_cast<volatile int*>(S.flags)[F_ABORT]) return false;
     const long long t0 = (p.trace && ct == 0) ? clock64() : 0;
-    uint32_t pending = 0;
+    int npairs = 0;
 #pragma unroll
-    for (int k = 0; k < MAX_EL; ++k)
-        if (ct + k * NCT < n) pending |= 1u << k;
+    for (int q = 0; q < NSEG; ++q) npairs += seg[q].n >> 1;
+    // address of the pair k of this thread (recomputed per poll: no pointer array held in registers)
+    auto at = [&](int k) -> const unsigned long long* {
+        int e = 2 * (ct + k * NCT);
+        const unsigned long long* a = seg[0].src + e;
+#pragma unroll
+        for (int q = 1; q < NSEG; ++q) {
+            e -= seg[q - 1].n;
+            if (e >= 0) a = seg[q].src + e;
+        }
+        return a;
+    };
+    uint32_t pending = 0;
+#pragma unroll 1
+    for (int k = 0; k < MAX_PR; ++k) {
+        if (ct + k * NCT < npairs) {
+            pending |= 1u << k;
+            // the gains are read once the values arrive: have them in L1 by then
+            if (gain) asm volatile("prefetch.global.L1 [%0];" ::"l"(gain + 2 * (ct + k * NCT)));
+        }
+    }
     float acc = 0.f;
     for (uint32_t it = 0; pending; ++it) {
+#pragma unroll 1
+        for (int k0 = 0; k0 < MAX_PR; k0 += PB) {
+            unsigned long long w0[PB], w1[PB];
 #pragma unroll
-        for (int k = 0; k < MAX_EL; ++k) {
-            if (pending & (1u << k)) {
-                const int i = ct + k * NCT;
-                const unsigned long long w = ll_load(ll + i);
-                if ((uint32_t)(w >> 32) == tag) {
-                    const float v = __uint_as_float((uint32_t)w);
-                    dst[i] = v;
-                    acc = fmaf(v, v, acc);
+            for (int kk = 0; kk < PB; ++kk) {
+                const int k = k0 + kk;
+                if (k < MAX_PR && (pending & (1u << k))) ll_load2(at(k), w0[kk], w1[kk]);
+            }
+#pragma unroll
+            for (int kk = 0; kk < PB; ++kk) {
+                const int k = k0 + kk;
+                if (k < MAX_PR && (pending & (1u << k)) && (uint32_t)(w0[kk] >> 32) == tag &&
+                    (uint32_t)(w1[kk] >> 32) == tag) {
+                    const float a = __uint_as_float((uint32_t)w0[kk]), b = __uint_as_float((uint32_t)w1[kk]);
+                    const int e = 2 * (ct + k * NCT);
+                    const uint32_t gp = gain ? __ldg(reinterpret_cast<const unsigned int*>(gain + e)) : 0x3f803f80u;
+                    *reinterpret_cast<float2*>(dst + (PERM ? xperm(e) : e)) = make_float2(a * bf_lo(gp), b * bf_hi(gp));
+                    acc = fmaf(a, a, fmaf(b, b, acc));
                     pending &= ~(1u << k);
                 }
             }
@@ -280,185 +344,249 @@ __device__ inline bool ll_fetch(const Ctx& S, const DecodeParams& p, const unsig
     return true;
 }
 
-// Input vector of a GEMV phase, optionally RMS-normalised with `gain`, into each warp's
-// registers xr (lane holds elements lane*8 + 256 i + j).  Source: `row` (bf16, the
-// embedding row) when non-null, else the tagged vector `ll`.  The staging buffer and the
-// reduction slots alternate between calls (`par`), so no trailing barrier is needed.
-template <int NI>
-__device__ inline void prep_input(const Ctx& S, const DecodeParams& p, const unsigned long long* ll,
-                                  const bf16_t* row, int n, uint32_t tag, const bf16_t* gain, float (&xr)[NI][8],
-                                  int& par) {
+// Input vector of a GEMV phase into shared memory, permuted (xperm): xs = gain * x (x
+// without a gain), and the RMSNorm scale r = rsqrt(mean x^2 + eps) (1 without a gain) that the
+// phase applies to its dot products, so rms_norm(x) * gain . w = r * (gain * x . w).
+// Source: `row` (bf16, the embedding row) when non-null, else the tagged vector `ll`.
+// The buffer and the reduction slots alternate between calls (`par`): a phase reads xs
+// until the next call's barrier, which every consumer thread passes first.
+__device__ inline float prep_input(const Ctx& S, const DecodeParams& p, const unsigned long long* ll,
+                                   const bf16_t* row, int n, uint32_t tag, const bf16_t* gain, const float*& xs,
+                                   int& par) {
     float* xb = S.xbuf + (size_t)par * S.kmax;
     float* rd = S.red + par * 8;
     par ^= 1;
     const int ct = threadIdx.x, warp = ct >> 5, lane = ct & 31;
-    uint4 gw[NI];   // gains in the register layout, loaded before the wait
-#pragma unroll
-    for (int i = 0; i < NI; ++i) {
-        const int k = lane * 8 + 256 * i;
-        gw[i] = (gain && k < n) ? *reinterpret_cast<const uint4*>(gain + k) : make_uint4(0, 0, 0, 0);
-    }
     float ss = 0.f;
     if (row) {
         for (int i = ct; i < n; i += NCT) {
             const float v = bf1(row[i]);
-            xb[i] = v;
+            xb[xperm(i)] = gain ? v * bf1(gain[i]) : v;
             ss = fmaf(v, v, ss);
         }
     } else {
-        ll_fetch(S, p, ll, n, tag, xb, &ss);
+        const LLSeg seg[1] = {{ll, n}};
+        ll_fetch<1, true>(S, p, seg, tag, xb, &ss, gain);
     }
     ss = warp_sum(ss);
     if (lane == 0) rd[warp] = ss;
     consumer_sync();
-    float r = 1.f;
-    if (gain) {
-        float tot = 0.f;
+    xs = xb;
+    if (!gain) return 1.f;
+    float tot = 0.f;
 #pragma unroll
-        for (int w = 0; w < NCW; ++w) tot += rd[w];
-        r = rsqrtf(tot / (float)n + p.eps);
-    }
-#pragma unroll
-    for (int i = 0; i < NI; ++i) {
-        const int k = lane * 8 + 256 * i;   // n is a multiple of 8: a lane's 8 values are all in or all out
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), b = a;
-        if (k < n) {
-            a = *reinterpret_cast<const float4*>(xb + k);
-            b = *reinterpret_cast<const float4*>(xb + k + 4);
-        }
-        if (gain) {
-            const uint4 g = gw[i];
-            a.x *= r * bf_lo(g.x); a.y *= r * bf_hi(g.x); a.z *= r * bf_lo(g.y); a.w *= r * bf_hi(g.y);
-            b.x *= r * bf_lo(g.z); b.y *= r * bf_hi(g.z); b.z *= r * bf_lo(g.w); b.w *= r * bf_hi(g.w);
-        }
-        xr[i][0] = a.x; xr[i][1] = a.y; xr[i][2] = a.z; xr[i][3] = a.w;
-        xr[i][4] = b.x; xr[i][5] = b.y; xr[i][6] = b.z; xr[i][7] = b.w;
-    }
+    for (int w = 0; w < NCW; ++w) tot += rd[w];
+    return rsqrtf(tot / (float)n + p.eps);
 }
 
-// Consumer view of the ring: every consumer warp walks the same stage sequence.
+// Consumer view of the ring: every consumer warp walks the same stage sequence.  The
+// slot and the barrier parity of the next stage are tracked incrementally (no division).
 struct Ring {
-    uint32_t stage = 0;   // next stage to consume
-    __device__ const char* slot_ptr(const Ctx& S, uint32_t st) const {
-        return S.ring + (size_t)(st % (uint32_t)S.nslot) * SLOT;
+    int slot = 0;          // slot of the next stage to consume
+    uint32_t parity = 0;   // parity of that slot's pending full-barrier phase
+    // Slot data of the stage d ahead of the next one (d < nslot).
+    __device__ const char* ptr(const Ctx& S, int d) const {
+        const int s = slot + d;
+        return S.ring + (size_t)(s >= S.nslot ? s - S.nslot : s) * SLOT;
     }
-    // Waits for stage st's data; after an abort it returns without waiting (the contents
-    // are then garbage, and nothing computed from them is published).
-    __device__ void wait_stage(const Ctx& S, const DecodeParams& p, uint32_t st) const {
-        const uint32_t slot = st % (uint32_t)S.nslot, round = st / (uint32_t)S.nslot;
+    // Waits for the data of the stage d ahead; after an abort it returns without waiting
+    // (the contents are then garbage, and nothing computed from them is published).
+    __device__ void wait(const Ctx& S, const DecodeParams& p, int d) const {
+        int s = slot + d;
+        uint32_t par = parity;
+        if (s >= S.nslot) {
+            s -= S.nslot;
+            par ^= 1u;
+        }
         const long long t0 = (p.trace && threadIdx.x == 0) ? clock64() : 0;
-        wait_bar(S, p, &S.full[slot], round & 1u, ERR_FULL);
+        wait_bar(S, p, &S.full[s], par, ERR_FULL);
         if (p.trace && threadIdx.x == 0) trace_add(S.flags, 0, (unsigned long long)(clock64() - t0));
     }
     __device__ const char* acquire(const Ctx& S, const DecodeParams& p) {
-        wait_stage(S, p, stage);
-        return slot_ptr(S, stage);
+        wait(S, p, 0);
+        return ptr(S, 0);
     }
     // After an abort a slot is never handed back: its copy may still be in flight, and the
     // producer must not reuse it (the final drain waits for it instead).
     __device__ void release(const Ctx& S) {
         __syncwarp();
         if ((threadIdx.x & 31) == 0 && !reinterpret_cast<volatile int*>(S.flags)[F_ABORT])
-            mbar_arrive(&S.empty[stage % (uint32_t)S.nslot]);
-        ++stage;
+            mbar_arrive(&S.empty[slot]);
+        if (++slot == S.nslot) {
+            slot = 0;
+            parity ^= 1u;
+        }
     }
 };
 
-// Rows [0, rows) of one matrix phase, spread over consecutive ring stages of `per` rows
-// (GLU: `per` gate/up pairs; a stage with n pairs holds n gate rows, then the n matching
-// up rows).  Up to 8 stages are acquired together; each warp then computes R rows at a
-// time with independent accumulators, so the dot products and the shuffle reductions of
-// several rows overlap.  emit(row, value) runs on lane 0; value is silu(gate) * up for GLU.
-// NK = number of 256-column chunks (K = 256 NK when EXACT).
-template <int NK, bool EXACT, bool GLU, int R, int NI, typename Emit>
-__device__ inline void phase_rows(Ring& ring, const Ctx& S, const DecodeParams& p, int rows, int per, int K,
-                                  const float (&xr)[NI][8], Emit emit, int group) {
-    static_assert(NK <= NI, "register vector too short");
+// Where the rows of a matrix phase go.
+enum { EMIT_LL = 0, EMIT_RESID = 1, EMIT_LOGITS = 2 };
+struct PhaseOut {
+    int kind;
+    unsigned long long* ll;   // EMIT_LL / EMIT_RESID: tagged destination of row 0
+    uint32_t tag;
+    float* logits;            // EMIT_LOGITS: logits of row 0
+    int row0;                 // EMIT_LOGITS: vocabulary index of row 0
+};
+
+// Row i's value v: a tagged element (EMIT_RESID first adds it into the residual row this
+// CTA owns), or a logit with the running (value, index) maximum of lane 0.
+__device__ __forceinline__ void emit_value(const Ctx& S, const PhaseOut& o, int i, float v, float& best, int& besti) {
+    if (o.kind == EMIT_LOGITS) {
+        o.logits[i] = v;
+        if (am_better(v, o.row0 + i, best, besti)) {
+            best = v;
+            besti = o.row0 + i;
+        }
+    } else {
+        if (o.kind == EMIT_RESID) {
+            v += S.xown[i];
+            S.xown[i] = v;
+        }
+        ll_store(o.ll + i, o.tag, v);
+    }
+}
+
+// Rows [r0, r1) of a matrix phase whose ring stages hold `per` rows each (GLU: `per`
+// gate/up pairs; a stage with n pairs holds n gate rows, then the n matching up rows);
+// stage s0 of the phase is the ring's next stage.  Each warp computes R rows at a time
+// with independent accumulators, so the dot products and the shuffle reductions of
+// several rows overlap.  The input vector xs is in shared memory; lane l covers columns
+// l*8 + 256 i.  Row values are r * (w . xs), or for GLU silu(r * gate . xs) * (r * up . xs).
+template <bool GLU, int R>
+__device__ inline void group_rows(const Ring& ring, const Ctx& S, int s0, int r0, int r1, int rows, int per,
+                                  float inv_per, int K, const float* xs, float r, const PhaseOut& out, float& best,
+                                  int& besti) {
     constexpr int NA = GLU ? 2 : 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int maxg = min(group, S.nslot - 1);
-    const int nst = (rows + per - 1) / per;
-    for (int s0 = 0; s0 < nst; s0 += maxg) {
-        const int g = min(maxg, nst - s0);
-        const uint32_t st0 = ring.stage;
-        for (int s = 0; s < g; ++s) ring.wait_stage(S, p, st0 + s);
-        const int r0 = s0 * per, r1 = min(rows, (s0 + g) * per);
-        for (int base = r0 + warp; base < r1; base += NCW * R) {
-            const uint4* w[R][NA];
-            bool valid[R];
+    for (int base = r0 + warp; base < r1; base += NCW * R) {
+        const uint4* w[R][NA];
+        bool valid[R];
 #pragma unroll
-            for (int j = 0; j < R; ++j) {
-                // rows past the end re-read row `base` (always valid): no branches in the dot products
-                const int rr = base + NCW * j;
-                valid[j] = rr < r1;
-                const int r = valid[j] ? rr : base;
-                const int st = r / per, off = r - st * per;
-                const int ns = min(per, rows - st * per);
-                const char* sp = ring.slot_ptr(S, st0 + (uint32_t)(st - s0));
-                w[j][0] = reinterpret_cast<const uint4*>(sp + (size_t)off * K * 2);
-                if (GLU) w[j][NA - 1] = reinterpret_cast<const uint4*>(sp + (size_t)(ns + off) * K * 2);
-            }
-            float acc[R][NA];
+        for (int j = 0; j < R; ++j) {
+            // rows past the end re-read row `base` (always valid): no branches in the dot products
+            const int rr = base + NCW * j;
+            valid[j] = rr < r1;
+            const int rw = valid[j] ? rr : base;
+            const int st = __float2int_rz(((float)rw + 0.5f) * inv_per), off = rw - st * per;
+            const int ns = min(per, rows - st * per);
+            const char* sp = ring.ptr(S, st - s0);
+            w[j][0] = reinterpret_cast<const uint4*>(sp + (size_t)off * K * 2);
+            if (GLU) w[j][NA - 1] = reinterpret_cast<const uint4*>(sp + (size_t)(ns + off) * K * 2);
+        }
+        float acc[R][NA];
+#pragma unroll
+        for (int j = 0; j < R; ++j)
+#pragma unroll
+            for (int a = 0; a < NA; ++a) acc[j][a] = 0.f;
+#pragma unroll 1
+        for (int c = 0; c * 256 + lane * 8 < K; ++c) {
+            float x[8];
+            load_x8(xs, c, lane, x);
+            const int k8 = c * 32 + lane;
 #pragma unroll
             for (int j = 0; j < R; ++j)
 #pragma unroll
-                for (int a = 0; a < NA; ++a) acc[j][a] = 0.f;
+                for (int a = 0; a < NA; ++a) acc[j][a] += dot8(w[j][a][k8], x);
+        }
 #pragma unroll
-            for (int i = 0; i < NK; ++i) {
-                const int k = lane * 8 + 256 * i;
-                if (EXACT || k < K) {
+        for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-                    for (int j = 0; j < R; ++j)
+            for (int j = 0; j < R; ++j)
 #pragma unroll
-                        for (int a = 0; a < NA; ++a) acc[j][a] += dot8(w[j][a][k >> 3], xr[i]);
-                }
-            }
+                for (int a = 0; a < NA; ++a) acc[j][a] += __shfl_xor_sync(0xffffffffu, acc[j][a], o);
+        // every lane holds every sum: lane j emits row j (the stores go out together)
+        float v = 0.f;
+        bool mine = false;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-                for (int j = 0; j < R; ++j)
-#pragma unroll
-                    for (int a = 0; a < NA; ++a) acc[j][a] += __shfl_xor_sync(0xffffffffu, acc[j][a], o);
-            if (lane == 0) {
-#pragma unroll
-                for (int j = 0; j < R; ++j)
-                    if (valid[j]) emit(base + NCW * j, GLU ? silu(acc[j][0]) * acc[j][NA - 1] : acc[j][0]);
+        for (int j = 0; j < R; ++j) {
+            if (lane == j) {
+                v = GLU ? silu(r * acc[j][0]) * (r * acc[j][NA - 1]) : r * acc[j][0];
+                mine = valid[j];
             }
         }
+        if (mine) emit_value(S, out, base + NCW * lane, v, best, besti);
+    }
+}
+
+// Rows [r0, r1) with K split over the warps: warp w takes the 256-column chunks w, w + NCW,
+// ... of every row in a block of up to KS_ROWS rows, so each warp reads its slice of the
+// input vector once; the warps' partial sums meet in shared memory and one thread per row
+// adds them and emits the row.  For groups with too few rows to give every warp whole rows
+// (o_proj, down_proj).  Every consumer thread calls it (it holds a barrier per block).
+__device__ inline void ksplit_rows(const Ring& ring, const Ctx& S, int s0, int r0, int r1, int per, float inv_per,
+                                   int K, const float* xs, float r, const PhaseOut& out, float& best, int& besti,
+                                   int& kpar) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int b0 = r0; b0 < r1; b0 += KS_ROWS) {
+        const int nr = min(KS_ROWS, r1 - b0);
+        const uint4* w[KS_ROWS];
+#pragma unroll
+        for (int j = 0; j < KS_ROWS; ++j) {
+            const int rw = b0 + min(j, nr - 1);
+            const int st = __float2int_rz(((float)rw + 0.5f) * inv_per), off = rw - st * per;
+            w[j] = reinterpret_cast<const uint4*>(ring.ptr(S, st - s0) + (size_t)off * K * 2);
+        }
+        float acc[KS_ROWS];
+#pragma unroll
+        for (int j = 0; j < KS_ROWS; ++j) acc[j] = 0.f;
+#pragma unroll 1
+        for (int c = warp; c * 256 < K; c += NCW) {
+            if (c * 256 + lane * 8 < K) {
+                float x[8];
+                load_x8(xs, c, lane, x);
+                const int k8 = c * 32 + lane;
+#pragma unroll
+                for (int j = 0; j < KS_ROWS; ++j)
+                    if (j < nr) acc[j] += dot8(w[j][k8], x);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int j = 0; j < KS_ROWS; ++j) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], o);
+        float* kr = S.kred + kpar * (NCW * KS_ROWS);
+        kpar ^= 1;
+        float v = 0.f;
+#pragma unroll
+        for (int j = 0; j < KS_ROWS; ++j)
+            if (lane == j) v = acc[j];
+        if (lane < KS_ROWS) kr[warp * KS_ROWS + lane] = v;
+        consumer_sync();
+        if ((int)threadIdx.x < nr) {
+            float t = 0.f;
+#pragma unroll
+            for (int q = 0; q < NCW; ++q) t += kr[q * KS_ROWS + threadIdx.x];
+            emit_value(S, out, b0 + threadIdx.x, r * t, best, besti);
+        }
+    }
+}
+
+// Rows [0, rows) of one matrix phase: up to `group` stages are acquired together (one wait,
+// then all their rows), then handed back.  The row routine is chosen per group: GLU pairs,
+// 4 rows a pass when the group has enough rows for every warp, K split over the warps
+// when it has few rows and a long K, else 1 row a pass.
+__device__ inline void gemv_phase(Ring& ring, const Ctx& S, const DecodeParams& p, bool glu, int rows, int per, int K,
+                                  const float* xs, float r, int group, const PhaseOut& out, float& best, int& besti,
+                                  int& kpar) {
+    const int maxg = min(group, S.nslot - 1);
+    const int nst = (rows + per - 1) / per;
+    // stage of row i = floor(i / per) as (i + 0.5) * (1 / per) truncated: exact for i < 2^20, per <= 2^10
+    const float inv_per = 1.f / (float)per;
+    for (int s0 = 0; s0 < nst; s0 += maxg) {
+        const int g = min(maxg, nst - s0);
+        for (int s = 0; s < g; ++s) ring.wait(S, p, s);
+        const int r0 = s0 * per, r1 = min(rows, (s0 + g) * per);
+        if (glu) group_rows<true, 3>(ring, S, s0, r0, r1, rows, per, inv_per, K, xs, r, out, best, besti);
+        else if (r1 - r0 >= 3 * NCW) group_rows<false, 4>(ring, S, s0, r0, r1, rows, per, inv_per, K, xs, r, out, best, besti);
+        else if (K >= 512 && r1 - r0 < 2 * NCW) ksplit_rows(ring, S, s0, r0, r1, per, inv_per, K, xs, r, out, best, besti, kpar);
+        else group_rows<false, 1>(ring, S, s0, r0, r1, rows, per, inv_per, K, xs, r, out, best, besti);
         for (int s = 0; s < g; ++s) ring.release(S);
     }
 }
 
-template <int NK, bool EXACT, bool GLU, int NI, typename Emit>
-__device__ inline void phase_rows_r(Ring& ring, const Ctx& S, const DecodeParams& p, int rows, int per, int K,
-                                    const float (&xr)[NI][8], Emit emit, int group) {
-    // several rows per warp pass when a stage group has them (independent accumulators
-    // overlap), fewer otherwise (clamped rows are wasted work)
-    const int rows_in_group = min(rows, min(group, S.nslot - 1) * per);
-    if (rows_in_group >= 3 * NCW) phase_rows<NK, EXACT, GLU, GLU ? 2 : 4>(ring, S, p, rows, per, K, xr, emit, group);
-    else if (rows_in_group >= 2 * NCW) phase_rows<NK, EXACT, GLU, 2>(ring, S, p, rows, per, K, xr, emit, group);
-    else phase_rows<NK, EXACT, GLU, 1>(ring, S, p, rows, per, K, xr, emit, group);
-}
-
-// `group`: stages acquired together (8 for latency-bound phases: one wait, then all the
-// rows; 3 for the bandwidth-bound lm_head, which hands slots back as it goes).
-template <bool GLU, int NI, typename Emit>
-__device__ inline void phase_any(Ring& ring, const Ctx& S, const DecodeParams& p, int rows, int per, int K,
-                                 const float (&xr)[NI][8], Emit emit, int group = 8) {
-    if constexpr (NI >= 12) {
-        if (K == 3072) { phase_rows_r<12, true, GLU>(ring, S, p, rows, per, K, xr, emit, group); return; }
-    }
-    if constexpr (NI >= 8) {
-        if (K == 2048) { phase_rows_r<8, true, GLU>(ring, S, p, rows, per, K, xr, emit, group); return; }
-    }
-    if constexpr (NI >= 4) {
-        if (K == 1024) { phase_rows_r<4, true, GLU>(ring, S, p, rows, per, K, xr, emit, group); return; }
-    }
-    phase_rows_r<NI, false, GLU>(ring, S, p, rows, per, K, xr, emit, group);
-}
-
 // ------------------------------------------------------------------ the kernel
-template <int D, int G, int NI>
+template <int D, int G>
 __global__ void __launch_bounds__(NT, 1) decode_persistent_kernel(const DecodeParams p) {
     extern __shared__ __align__(1024) char smem[];
     const int nc = gridDim.x, c = blockIdx.x;
@@ -475,9 +603,10 @@ __global__ void __launch_bounds__(NT, 1) decode_persistent_kernel(const DecodePa
     S.xown = reinterpret_cast<float*>(smem + LO.xown);
     S.att = reinterpret_cast<float*>(smem + LO.att);
     S.red = reinterpret_cast<float*>(smem + LO.red);
+    S.kred = reinterpret_cast<float*>(smem + LO.kred);
     S.flags = reinterpret_cast<int*>(smem + LO.flags);
     S.nslot = p.nslot;
-    S.kmax = kmax;
+    S.kmax = xbuf_floats(kmax);
     const Plan P = make_plan(p, c, nc);
     const uint32_t tags_per_step = (uint32_t)p.NL * PH_PER_LAYER + 1;
     auto tag = [&](int l, int ph) { return p.epoch * tags_per_step + (uint32_t)(l * PH_PER_LAYER + ph); };
@@ -501,61 +630,66 @@ __global__ void __launch_bounds__(NT, 1) decode_persistent_kernel(const DecodePa
     if (warp == NCW) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            uint32_t stage = 0;
+            // One pass over the step's phases in consumption order; each phase is described
+            // by its source rows [i0, i1) (`per` a stage, `stride` elements apart) and either
+            // two stages per item group (a K chunk, then its V chunk) or one stage with two
+            // sources (gate rows, then the matching up rows).
+            int slot = 0, issued = 0;
+            uint32_t parity = 0;
             bool ok = true;
-            auto issue = [&](const void* s0, uint32_t b0, const void* s1, uint32_t b1) {
-                if (!ok) return;
-                const uint32_t slot = stage % (uint32_t)S.nslot, round = stage / (uint32_t)S.nslot;
-                if (!wait_bar(S, p, &S.empty[slot], (round & 1u) ^ 1u, ERR_EMPTY) ||
-                    reinterpret_cast<volatile int*>(S.flags)[F_ABORT]) {
-                    ok = false;
-                    return;
+            const int n_ph = p.NL * PH_PER_LAYER + 1;
+#pragma unroll 1
+            for (int t = 0; t < n_ph && ok; ++t) {
+                const int l = min(t / PH_PER_LAYER, p.NL - 1);
+                const int e = (t == n_ph - 1) ? PH_PER_LAYER : t - l * PH_PER_LAYER;
+                const DecodeLayer* Lw = p.layers + l;
+                const bf16_t *src0, *src1 = nullptr, *src_up = nullptr;
+                int i0, i1, per, stride, nsub = 1;
+                if (e == 0) {
+                    src0 = Lw->wqkv; i0 = P.q0; i1 = P.q1; per = P.rps_h; stride = p.H;
+                } else if (e == 1) {
+                    const size_t off = (size_t)P.ug * p.max_seq * D;
+                    src0 = Lw->kc + off; src1 = Lw->vc + off; i0 = P.c0; i1 = P.old_end; per = P.pps_kv; stride = D;
+                    nsub = 2;
+                } else if (e == 2) {
+                    src0 = Lw->wo; i0 = P.x0; i1 = P.x1; per = P.rps_o; stride = HQD;
+                } else if (e == 3) {
+                    src0 = Lw->wgu; src_up = Lw->wgu + (size_t)p.F * p.H; i0 = P.f0; i1 = P.f1; per = P.pps_gu;
+                    stride = p.H;
+                } else if (e == 4) {
+                    src0 = Lw->wd; i0 = P.x0; i1 = P.x1; per = P.rps_f; stride = p.F;
+                } else {
+                    src0 = p.embed; i0 = P.v0; i1 = P.v1; per = P.rps_h; stride = p.H;
                 }
-                mbar_expect_tx(&S.full[slot], b0 + b1);
-                char* dst = S.ring + (size_t)slot * SLOT;
-                tma_load_1d(dst, s0, b0, &S.full[slot]);
-                if (b1) tma_load_1d(dst + b0, s1, b1, &S.full[slot]);
-                ++stage;
-            };
-            for (int l = 0; l < p.NL && ok; ++l) {
-                const DecodeLayer Lw = p.layers[l];   // by value: registers survive the asm memory clobbers
-                for (int r = P.q0; r < P.q1; r += P.rps_h) {
-                    const int n = min(P.rps_h, P.q1 - r);
-                    issue(Lw.wqkv + (size_t)r * p.H, (uint32_t)n * p.H * 2, nullptr, 0);
+                for (int i = i0; i < i1 && ok; i += per) {
+                    const uint32_t bytes = (uint32_t)min(per, i1 - i) * (uint32_t)stride * 2u;
+                    for (int sub = 0; sub < nsub; ++sub) {
+                        if (!wait_bar(S, p, &S.empty[slot], parity ^ 1u, ERR_EMPTY) ||
+                            reinterpret_cast<volatile int*>(S.flags)[F_ABORT]) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_expect_tx(&S.full[slot], src_up ? 2u * bytes : bytes);
+                        char* dst = S.ring + (size_t)slot * SLOT;
+                        tma_load_1d(dst, (sub == 0 ? src0 : src1) + (size_t)i * stride, bytes, &S.full[slot]);
+                        if (src_up) tma_load_1d(dst + bytes, src_up + (size_t)i * stride, bytes, &S.full[slot]);
+                        ++issued;
+                        if (++slot == S.nslot) {
+                            slot = 0;
+                            parity ^= 1u;
+                        }
+                    }
                 }
-                for (int q = P.c0; q < P.old_end; q += P.pps_kv) {
-                    const int n = min(P.pps_kv, P.old_end - q);
-                    const size_t off = ((size_t)P.ug * p.max_seq + q) * D;
-                    issue(Lw.kc + off, (uint32_t)n * D * 2, nullptr, 0);
-                    issue(Lw.vc + off, (uint32_t)n * D * 2, nullptr, 0);
-                }
-                for (int r = P.x0; r < P.x1; r += P.rps_o) {
-                    const int n = min(P.rps_o, P.x1 - r);
-                    issue(Lw.wo + (size_t)r * HQD, (uint32_t)n * HQD * 2, nullptr, 0);
-                }
-                for (int j = P.f0; j < P.f1; j += P.pps_gu) {
-                    const int n = min(P.pps_gu, P.f1 - j);
-                    issue(Lw.wgu + (size_t)j * p.H, (uint32_t)n * p.H * 2, Lw.wgu + (size_t)(p.F + j) * p.H,
-                          (uint32_t)n * p.H * 2);
-                }
-                for (int r = P.x0; r < P.x1; r += P.rps_f) {
-                    const int n = min(P.rps_f, P.x1 - r);
-                    issue(Lw.wd + (size_t)r * p.F, (uint32_t)n * p.F * 2, nullptr, 0);
-                }
-                trace_mark(p, 10 * p.NL + 4 + l);
+                if (e == 4) trace_mark(p, 10 * p.NL + 4 + l);
             }
-            for (int r = P.v0; r < P.v1 && ok; r += P.rps_h) {
-                const int n = min(P.rps_h, P.v1 - r);
-                issue(p.embed + (size_t)r * p.H, (uint32_t)n * p.H * 2, nullptr, 0);
-            }
-            reinterpret_cast<volatile int*>(S.flags)[F_ISSUED] = (int)stage;
+            reinterpret_cast<volatile int*>(S.flags)[F_ISSUED] = issued;
         }
     } else {
         // ------------------------------------------------------------ consumers
         // Control flow below depends only on the plan, never on errors: every consumer
         // thread executes the same barriers whatever happens.
         Ring ring;
-        float xr[NI][8];
+        const float* xs = nullptr;   // input vector of the current phase (shared memory)
         int par = 0;   // alternates the staging buffer between input preparations
         if (c == 0 && threadIdx.x == 0) p.history[p.pos] = token;
         for (int r = P.x0 + threadIdx.x; r < P.x1; r += NCT) S.xown[r - P.x0] = bf1(erow[r]);
@@ -563,318 +697,319 @@ __global__ void __launch_bounds__(NT, 1) decode_persistent_kernel(const DecodePa
         const bool tr = p.trace && threadIdx.x == 0;
         if (tr) trace_mark(p, 10 * p.NL + 0);
 
-        for (int l = 0; l < p.NL; ++l) {
-            const DecodeLayer Lw = p.layers[l];   // by value: registers survive the asm memory clobbers
-            // ---- P1: QKV rows (input: rms_norm(x) * g_in) -> tagged qkv
-            if (P.q1 > P.q0) {
-                prep_input<NI>(S, p, p.ll_x, l == 0 ? erow : nullptr, p.H, l == 0 ? 0u : tag(l - 1, PH_X2),
-                               Lw.g_in, xr, par);
-                if (tr) trace_mark(p, l * 10 + 0);
-                const uint32_t t = tag(l, PH_QKV);
-                unsigned long long* dst = p.ll_qkv + P.q0;
-                phase_any<false>(ring, S, p, P.q1 - P.q0, P.rps_h, p.H, xr,
-                                 [&](int i, float v) { ll_store(dst + i, t, v); });
-                if (tr) trace_mark(p, l * 10 + 1);
-            }
-            // ---- P2: attention unit (kv head ug, key chunk [c0, c1))
-            if (P.unit) {
-                constexpr int EPL = D / 32;
-                const int g = P.ug;
-                const uint32_t tq = tag(l, PH_QKV);
-                const int half = D / 2;
-                constexpr int PPL = (D / 2 + 31) / 32;   // NeoX pairs per lane
-                // gains and cos/sin of the first head this warp normalises, loaded before the waits
-                float pg_a[PPL], pg_b[PPL];
-                float2 pcs[PPL];
-                {
-                    const bf16_t* gn0 = warp < G ? Lw.g_q : Lw.g_k;
-#pragma unroll
-                    for (int k = 0; k < PPL; ++k) {
-                        const int i = lane + 32 * k;
-                        pg_a[k] = i < half ? bf1(gn0[i]) : 0.f;
-                        pg_b[k] = i < half ? bf1(gn0[i + half]) : 0.f;
-                        pcs[k] = i < half ? p.rope[(size_t)p.pos * half + i] : make_float2(1.f, 0.f);
-                    }
-                }
-                float ss = 0.f;
-                float* xa = S.xbuf + (size_t)par * S.kmax;   // q heads, then k, then v
-                par ^= 1;
-                ll_fetch(S, p, p.ll_qkv + (size_t)g * G * D, G * D, tq, xa, &ss);
-                ll_fetch(S, p, p.ll_qkv + HQD + (size_t)g * D, D, tq, xa + G * D, &ss);
-                ll_fetch(S, p, p.ll_qkv + HQD + (size_t)(p.HKV + g) * D, D, tq, xa + (G + 1) * D, &ss);
-                consumer_sync();
-                if (tr) trace_mark(p, l * 10 + 2);
-                // per-head RMSNorm + NeoX RoPE on the G q heads and the k head; bf16 rounding of k, v
-                for (int hh = warp; hh <= G; hh += NCW) {
-                    float* hv = xa + hh * D;
-                    if (hh != warp) {   // a second head for this warp (G + 1 > NCW): load its gains now
-                        const bf16_t* gn1 = hh < G ? Lw.g_q : Lw.g_k;
-#pragma unroll
+        float best = -INFINITY;   // lm_head: this thread's running maximum of the rows it emitted
+        int besti = 0x7fffffff;
+        int kpar = 0;             // alternates the K-split partial buffers
+        // One pass over the step's phases: per layer QKV rows, attention, o_proj rows,
+        // gate_up pairs, down_proj rows; then the lm_head rows.  A single copy of each code
+        // path serves every phase (the loop is not unrolled), which keeps the kernel's hot
+        // code small enough to stay in the instruction cache.
+        const int n_ph = p.NL * PH_PER_LAYER + 1;
+#pragma unroll 1
+        for (int t = 0; t < n_ph; ++t) {
+            const int l = min(t / PH_PER_LAYER, p.NL - 1);
+            const int e = (t == n_ph - 1) ? PH_PER_LAYER : t - l * PH_PER_LAYER;
+            const DecodeLayer* Lw = p.layers + l;
+            if (e == PH_O) {
+                // ---- attention unit (kv head ug, key chunk [c0, c1)) -> tagged o
+                if (P.unit) {
+                    constexpr int EPL = D / 32;
+                    const int g = P.ug;
+                    const uint32_t tq = tag(l, PH_QKV);
+                    const int half = D / 2;
+                    constexpr int PPL = (D / 2 + 31) / 32;   // NeoX pairs per lane
+                    // gains and cos/sin of the first head this warp normalises, loaded before the waits
+                    float pg_a[PPL], pg_b[PPL];
+                    float2 pcs[PPL];
+                    {
+                        const bf16_t* gn0 = warp < G ? Lw->g_q : Lw->g_k;
+    #pragma unroll
                         for (int k = 0; k < PPL; ++k) {
                             const int i = lane + 32 * k;
-                            pg_a[k] = i < half ? bf1(gn1[i]) : 0.f;
-                            pg_b[k] = i < half ? bf1(gn1[i + half]) : 0.f;
+                            pg_a[k] = i < half ? bf1(gn0[i]) : 0.f;
+                            pg_b[k] = i < half ? bf1(gn0[i + half]) : 0.f;
+                            pcs[k] = i < half ? p.rope[(size_t)p.pos * half + i] : make_float2(1.f, 0.f);
                         }
                     }
-                    float a[PPL], b[PPL];
-                    float s2 = 0.f;
-#pragma unroll
-                    for (int k = 0; k < PPL; ++k) {
-                        const int i = lane + 32 * k;
-                        a[k] = i < half ? hv[i] : 0.f;
-                        b[k] = i < half ? hv[i + half] : 0.f;
-                        s2 += a[k] * a[k] + b[k] * b[k];
-                    }
-                    s2 = warp_sum(s2);
-                    const float r = rsqrtf(s2 / (float)D + p.eps);
-#pragma unroll
-                    for (int k = 0; k < PPL; ++k) {
-                        const int i = lane + 32 * k;
-                        if (i < half) {
-                            const float x1 = a[k] * r * pg_a[k], x2 = b[k] * r * pg_b[k];
-                            const float2 cs = pcs[k];
-                            float o1 = x1 * cs.x - x2 * cs.y, o2 = x2 * cs.x + x1 * cs.y;
-                            if (hh == G) {   // the cache holds bf16 keys: use the rounded values
-                                o1 = bf1(f2bf(o1));
-                                o2 = bf1(f2bf(o2));
+                    float ss = 0.f;
+                    float* xa = S.xbuf + (size_t)par * S.kmax;   // q heads, then k, then v
+                    par ^= 1;
+                    const LLSeg seg[3] = {{p.ll_qkv + (size_t)g * G * D, G * D},
+                                          {p.ll_qkv + HQD + (size_t)g * D, D},
+                                          {p.ll_qkv + HQD + (size_t)(p.HKV + g) * D, D}};
+                    ll_fetch(S, p, seg, tq, xa, &ss);
+                    consumer_sync();
+                    if (tr) trace_mark(p, l * 10 + 2);
+                    // per-head RMSNorm + NeoX RoPE on the G q heads and the k head; bf16 rounding of k, v
+                    for (int hh = warp; hh <= G; hh += NCW) {
+                        float* hv = xa + hh * D;
+                        if (hh != warp) {   // a second head for this warp (G + 1 > NCW): load its gains now
+                            const bf16_t* gn1 = hh < G ? Lw->g_q : Lw->g_k;
+    #pragma unroll
+                            for (int k = 0; k < PPL; ++k) {
+                                const int i = lane + 32 * k;
+                                pg_a[k] = i < half ? bf1(gn1[i]) : 0.f;
+                                pg_b[k] = i < half ? bf1(gn1[i + half]) : 0.f;
                             }
-                            hv[i] = o1;
-                            hv[i + half] = o2;
+                        }
+                        float a[PPL], b[PPL];
+                        float s2 = 0.f;
+    #pragma unroll
+                        for (int k = 0; k < PPL; ++k) {
+                            const int i = lane + 32 * k;
+                            a[k] = i < half ? hv[i] : 0.f;
+                            b[k] = i < half ? hv[i + half] : 0.f;
+                            s2 += a[k] * a[k] + b[k] * b[k];
+                        }
+                        s2 = warp_sum(s2);
+                        const float r = rsqrtf(s2 / (float)D + p.eps);
+    #pragma unroll
+                        for (int k = 0; k < PPL; ++k) {
+                            const int i = lane + 32 * k;
+                            if (i < half) {
+                                const float x1 = a[k] * r * pg_a[k], x2 = b[k] * r * pg_b[k];
+                                const float2 cs = pcs[k];
+                                float o1 = x1 * cs.x - x2 * cs.y, o2 = x2 * cs.x + x1 * cs.y;
+                                if (hh == G) {   // the cache holds bf16 keys: use the rounded values
+                                    o1 = bf1(f2bf(o1));
+                                    o2 = bf1(f2bf(o2));
+                                }
+                                hv[i] = o1;
+                                hv[i + half] = o2;
+                            }
                         }
                     }
-                }
-                for (int d = threadIdx.x; d < D; d += NCT) xa[(G + 1) * D + d] = bf1(f2bf(xa[(G + 1) * D + d]));
-                consumer_sync();
-                const bool has_new = (P.c0 <= p.pos) && (p.pos < P.c1);
-                if (has_new) {
-                    for (int d = threadIdx.x; d < D; d += NCT) {
-                        Lw.kc[((size_t)g * p.max_seq + p.pos) * D + d] = f2bf(xa[G * D + d]);
-                        Lw.vc[((size_t)g * p.max_seq + p.pos) * D + d] = f2bf(xa[(G + 1) * D + d]);
+                    for (int d = threadIdx.x; d < D; d += NCT) xa[(G + 1) * D + d] = bf1(f2bf(xa[(G + 1) * D + d]));
+                    consumer_sync();
+                    const bool has_new = (P.c0 <= p.pos) && (p.pos < P.c1);
+                    if (has_new) {
+                        for (int d = threadIdx.x; d < D; d += NCT) {
+                            Lw->kc[((size_t)g * p.max_seq + p.pos) * D + d] = f2bf(xa[G * D + d]);
+                            Lw->vc[((size_t)g * p.max_seq + p.pos) * D + d] = f2bf(xa[(G + 1) * D + d]);
+                        }
                     }
-                }
-                const float scale = rsqrtf((float)D);
-                float qv[G][EPL], m[G], lsum[G], o[G][EPL];
-#pragma unroll
-                for (int gi = 0; gi < G; ++gi) {
-#pragma unroll
-                    for (int e = 0; e < EPL; ++e) {
-                        qv[gi][e] = xa[gi * D + lane * EPL + e] * scale;
-                        o[gi][e] = 0.f;
+                    const float scale = rsqrtf((float)D);
+                    float qv[G][EPL], m[G], lsum[G], o[G][EPL];
+    #pragma unroll
+                    for (int gi = 0; gi < G; ++gi) {
+    #pragma unroll
+                        for (int e = 0; e < EPL; ++e) {
+                            qv[gi][e] = xa[gi * D + lane * EPL + e] * scale;
+                            o[gi][e] = 0.f;
+                        }
+                        m[gi] = -INFINITY;
+                        lsum[gi] = 0.f;
                     }
-                    m[gi] = -INFINITY;
-                    lsum[gi] = 0.f;
-                }
-                // online softmax over the streamed keys: per stage, warp w takes positions w + NCW k
-                constexpr int KPW = (64 + NCW - 1) / NCW;   // positions per warp per stage (pps_kv <= 64)
-                for (int q = P.c0; q < P.old_end; q += P.pps_kv) {
-                    const int np = min(P.pps_kv, P.old_end - q);
-                    const char* ks = ring.acquire(S, p);
-                    float s[KPW][G];
-#pragma unroll
-                    for (int k = 0; k < KPW; ++k) {
-                        const int t = min(warp + NCW * k, np - 1);   // clamped: computed, then masked
-                        float kf[EPL];
-                        load_lane_bf16<EPL>(reinterpret_cast<const bf16_t*>(ks) + (size_t)t * D, lane, kf);
-#pragma unroll
+                    // online softmax over the streamed keys: per stage, warp w takes positions w + NCW k
+                    constexpr int KPW = (64 + NCW - 1) / NCW;   // positions per warp per stage (pps_kv <= 64)
+                    for (int q = P.c0; q < P.old_end; q += P.pps_kv) {
+                        const int np = min(P.pps_kv, P.old_end - q);
+                        const char* ks = ring.acquire(S, p);
+                        float s[KPW][G];
+    #pragma unroll
+                        for (int k = 0; k < KPW; ++k) {
+                            const int t = min(warp + NCW * k, np - 1);   // clamped: computed, then masked
+                            float kf[EPL];
+                            load_lane_bf16<EPL>(reinterpret_cast<const bf16_t*>(ks) + (size_t)t * D, lane, kf);
+    #pragma unroll
+                            for (int gi = 0; gi < G; ++gi) {
+                                float d0 = 0.f;
+    #pragma unroll
+                                for (int e = 0; e < EPL; ++e) d0 = fmaf(qv[gi][e], kf[e], d0);
+                                s[k][gi] = d0;
+                            }
+                        }
+    #pragma unroll
+                        for (int sh = 16; sh > 0; sh >>= 1)
+    #pragma unroll
+                            for (int k = 0; k < KPW; ++k)
+    #pragma unroll
+                                for (int gi = 0; gi < G; ++gi) s[k][gi] += __shfl_xor_sync(0xffffffffu, s[k][gi], sh);
+    #pragma unroll
+                        for (int k = 0; k < KPW; ++k)
+                            if (warp + NCW * k >= np)
+    #pragma unroll
+                                for (int gi = 0; gi < G; ++gi) s[k][gi] = -INFINITY;
+                        ring.release(S);
+    #pragma unroll
+                        for (int gi = 0; gi < G; ++gi) {
+                            float mx = -INFINITY;
+    #pragma unroll
+                            for (int k = 0; k < KPW; ++k) mx = fmaxf(mx, s[k][gi]);
+                            const float mn = fmaxf(m[gi], mx);
+                            if (mn != -INFINITY) {
+                                const float corr = expf(m[gi] - mn);   // 0 when m was -inf
+                                lsum[gi] *= corr;
+    #pragma unroll
+                                for (int e = 0; e < EPL; ++e) o[gi][e] *= corr;
+                                m[gi] = mn;
+    #pragma unroll
+                                for (int k = 0; k < KPW; ++k) {
+                                    s[k][gi] = (s[k][gi] == -INFINITY) ? 0.f : expf(s[k][gi] - mn);
+                                    lsum[gi] += s[k][gi];
+                                }
+                            } else {
+    #pragma unroll
+                                for (int k = 0; k < KPW; ++k) s[k][gi] = 0.f;
+                            }
+                        }
+                        const char* vs = ring.acquire(S, p);
+    #pragma unroll
+                        for (int k = 0; k < KPW; ++k) {
+                            const int t = min(warp + NCW * k, np - 1);   // masked positions carry weight 0
+                            float vf[EPL];
+                            load_lane_bf16<EPL>(reinterpret_cast<const bf16_t*>(vs) + (size_t)t * D, lane, vf);
+    #pragma unroll
+                            for (int gi = 0; gi < G; ++gi)
+    #pragma unroll
+                                for (int e = 0; e < EPL; ++e) o[gi][e] = fmaf(s[k][gi], vf[e], o[gi][e]);
+                        }
+                        ring.release(S);
+                    }
+                    if (has_new && warp == 0) {   // the token's own key and value
+                        float kf[EPL], vf[EPL];
+    #pragma unroll
+                        for (int e = 0; e < EPL; ++e) {
+                            kf[e] = xa[G * D + lane * EPL + e];
+                            vf[e] = xa[(G + 1) * D + lane * EPL + e];
+                        }
+    #pragma unroll
                         for (int gi = 0; gi < G; ++gi) {
                             float d0 = 0.f;
-#pragma unroll
+    #pragma unroll
                             for (int e = 0; e < EPL; ++e) d0 = fmaf(qv[gi][e], kf[e], d0);
-                            s[k][gi] = d0;
-                        }
-                    }
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-                        for (int k = 0; k < KPW; ++k)
-#pragma unroll
-                            for (int gi = 0; gi < G; ++gi) s[k][gi] += __shfl_xor_sync(0xffffffffu, s[k][gi], o);
-#pragma unroll
-                    for (int k = 0; k < KPW; ++k)
-                        if (warp + NCW * k >= np)
-#pragma unroll
-                            for (int gi = 0; gi < G; ++gi) s[k][gi] = -INFINITY;
-                    ring.release(S);
-#pragma unroll
-                    for (int gi = 0; gi < G; ++gi) {
-                        float mx = -INFINITY;
-#pragma unroll
-                        for (int k = 0; k < KPW; ++k) mx = fmaxf(mx, s[k][gi]);
-                        const float mn = fmaxf(m[gi], mx);
-                        if (mn != -INFINITY) {
-                            const float corr = expf(m[gi] - mn);   // 0 when m was -inf
-                            lsum[gi] *= corr;
-#pragma unroll
-                            for (int e = 0; e < EPL; ++e) o[gi][e] *= corr;
+                            const float sc = warp_sum(d0);
+                            const float mn = fmaxf(m[gi], sc);
+                            const float corr = expf(m[gi] - mn);
+                            const float pr = expf(sc - mn);
+                            lsum[gi] = lsum[gi] * corr + pr;
+    #pragma unroll
+                            for (int e = 0; e < EPL; ++e) o[gi][e] = fmaf(pr, vf[e], o[gi][e] * corr);
                             m[gi] = mn;
-#pragma unroll
-                            for (int k = 0; k < KPW; ++k) {
-                                s[k][gi] = (s[k][gi] == -INFINITY) ? 0.f : expf(s[k][gi] - mn);
-                                lsum[gi] += s[k][gi];
-                            }
-                        } else {
-#pragma unroll
-                            for (int k = 0; k < KPW; ++k) s[k][gi] = 0.f;
                         }
                     }
-                    const char* vs = ring.acquire(S, p);
-#pragma unroll
-                    for (int k = 0; k < KPW; ++k) {
-                        const int t = min(warp + NCW * k, np - 1);   // masked positions carry weight 0
-                        float vf[EPL];
-                        load_lane_bf16<EPL>(reinterpret_cast<const bf16_t*>(vs) + (size_t)t * D, lane, vf);
-#pragma unroll
-                        for (int gi = 0; gi < G; ++gi)
-#pragma unroll
-                            for (int e = 0; e < EPL; ++e) o[gi][e] = fmaf(s[k][gi], vf[e], o[gi][e]);
-                    }
-                    ring.release(S);
-                }
-                if (has_new && warp == 0) {   // the token's own key and value
-                    float kf[EPL], vf[EPL];
-#pragma unroll
-                    for (int e = 0; e < EPL; ++e) {
-                        kf[e] = xa[G * D + lane * EPL + e];
-                        vf[e] = xa[(G + 1) * D + lane * EPL + e];
-                    }
-#pragma unroll
+                    // merge the warps' (m, l, o)
+    #pragma unroll
                     for (int gi = 0; gi < G; ++gi) {
-                        float d0 = 0.f;
-#pragma unroll
-                        for (int e = 0; e < EPL; ++e) d0 = fmaf(qv[gi][e], kf[e], d0);
-                        const float sc = warp_sum(d0);
-                        const float mn = fmaxf(m[gi], sc);
-                        const float corr = expf(m[gi] - mn);
-                        const float pr = expf(sc - mn);
-                        lsum[gi] = lsum[gi] * corr + pr;
-#pragma unroll
-                        for (int e = 0; e < EPL; ++e) o[gi][e] = fmaf(pr, vf[e], o[gi][e] * corr);
-                        m[gi] = mn;
-                    }
-                }
-                // merge the warps' (m, l, o)
-#pragma unroll
-                for (int gi = 0; gi < G; ++gi) {
-                    float* a = S.att + ((size_t)warp * G + gi) * (D + 2);
-                    if (lane == 0) {
-                        a[0] = m[gi];
-                        a[1] = lsum[gi];
-                    }
-#pragma unroll
-                    for (int e = 0; e < EPL; ++e) a[2 + lane * EPL + e] = o[gi][e];
-                }
-                consumer_sync();
-                const uint32_t to = tag(l, PH_O);
-                const bool single = p.n_chunks == 1;
-                for (int idx = threadIdx.x; idx < G * D; idx += NCT) {
-                    const int gi = idx / D, d = idx % D;
-                    float M = -INFINITY;
-#pragma unroll
-                    for (int w = 0; w < NCW; ++w) M = fmaxf(M, S.att[((size_t)w * G + gi) * (D + 2)]);
-                    float lt = 0.f, ot = 0.f;
-#pragma unroll
-                    for (int w = 0; w < NCW; ++w) {
-                        const float* a = S.att + ((size_t)w * G + gi) * (D + 2);
-                        const float f = (a[0] == -INFINITY) ? 0.f : expf(a[0] - M);
-                        lt += f * a[1];
-                        ot += f * a[2 + d];
-                    }
-                    const int h = g * G + gi;
-                    if (single) {
-                        ll_store(p.ll_o + (size_t)h * D + d, to, ot / lt);
-                    } else {
-                        float* part = p.attn_part + ((size_t)h * p.n_chunks + P.uj) * (D + 2);
-                        part[2 + d] = ot;
-                        if (d == 0) {
-                            part[0] = M;
-                            part[1] = lt;
+                        float* a = S.att + ((size_t)warp * G + gi) * (D + 2);
+                        if (lane == 0) {
+                            a[0] = m[gi];
+                            a[1] = lsum[gi];
                         }
-                    }
-                }
-                if (!single) {
-                    __threadfence();
-                    consumer_sync();
-                    if (threadIdx.x == 0) {
-                        const unsigned int tk = atomicAdd(&p.attn_count[l * p.HKV + g], 1u);
-                        S.flags[2] = (tk == (unsigned int)p.n_chunks - 1) ? 1 : 0;
+    #pragma unroll
+                        for (int e = 0; e < EPL; ++e) a[2 + lane * EPL + e] = o[gi][e];
                     }
                     consumer_sync();
-                    if (S.flags[2]) {   // the last chunk of this kv head merges all chunks
-                        __threadfence();
-                        for (int idx = threadIdx.x; idx < G * D; idx += NCT) {
-                            const int gi = idx / D, d = idx % D;
-                            const int h = g * G + gi;
-                            const float* base = p.attn_part + (size_t)h * p.n_chunks * (D + 2);
-                            float M = -INFINITY;
-                            for (int j = 0; j < p.n_chunks; ++j) M = fmaxf(M, __ldcg(base + (size_t)j * (D + 2)));
-                            float lt = 0.f, ot = 0.f;
-                            for (int j = 0; j < p.n_chunks; ++j) {
-                                const float* a = base + (size_t)j * (D + 2);
-                                const float mj = __ldcg(a);
-                                const float f = (mj == -INFINITY) ? 0.f : expf(mj - M);
-                                lt += f * __ldcg(a + 1);
-                                ot += f * __ldcg(a + 2 + d);
-                            }
+                    const uint32_t to = tag(l, PH_O);
+                    const bool single = p.n_chunks == 1;
+                    for (int idx = threadIdx.x; idx < G * D; idx += NCT) {
+                        const int gi = idx / D, d = idx % D;
+                        float M = -INFINITY;
+    #pragma unroll
+                        for (int w = 0; w < NCW; ++w) M = fmaxf(M, S.att[((size_t)w * G + gi) * (D + 2)]);
+                        float lt = 0.f, ot = 0.f;
+    #pragma unroll
+                        for (int w = 0; w < NCW; ++w) {
+                            const float* a = S.att + ((size_t)w * G + gi) * (D + 2);
+                            const float f = (a[0] == -INFINITY) ? 0.f : expf(a[0] - M);
+                            lt += f * a[1];
+                            ot += f * a[2 + d];
+                        }
+                        const int h = g * G + gi;
+                        if (single) {
                             ll_store(p.ll_o + (size_t)h * D + d, to, ot / lt);
+                        } else {
+                            float* part = p.attn_part + ((size_t)h * p.n_chunks + P.uj) * (D + 2);
+                            part[2 + d] = ot;
+                            if (d == 0) {
+                                part[0] = M;
+                                part[1] = lt;
+                            }
                         }
-                        if (threadIdx.x == 0) p.attn_count[l * p.HKV + g] = 0u;
                     }
+                    if (!single) {
+                        __threadfence();
+                        consumer_sync();
+                        if (threadIdx.x == 0) {
+                            const unsigned int tk = atomicAdd(&p.attn_count[l * p.HKV + g], 1u);
+                            S.flags[2] = (tk == (unsigned int)p.n_chunks - 1) ? 1 : 0;
+                        }
+                        consumer_sync();
+                        if (S.flags[2]) {   // the last chunk of this kv head merges all chunks
+                            __threadfence();
+                            for (int idx = threadIdx.x; idx < G * D; idx += NCT) {
+                                const int gi = idx / D, d = idx % D;
+                                const int h = g * G + gi;
+                                const float* base = p.attn_part + (size_t)h * p.n_chunks * (D + 2);
+                                float M = -INFINITY;
+                                for (int j = 0; j < p.n_chunks; ++j) M = fmaxf(M, __ldcg(base + (size_t)j * (D + 2)));
+                                float lt = 0.f, ot = 0.f;
+                                for (int j = 0; j < p.n_chunks; ++j) {
+                                    const float* a = base + (size_t)j * (D + 2);
+                                    const float mj = __ldcg(a);
+                                    const float f = (mj == -INFINITY) ? 0.f : expf(mj - M);
+                                    lt += f * __ldcg(a + 1);
+                                    ot += f * __ldcg(a + 2 + d);
+                                }
+                                ll_store(p.ll_o + (size_t)h * D + d, to, ot / lt);
+                            }
+                            if (threadIdx.x == 0) p.attn_count[l * p.HKV + g] = 0u;
+                        }
+                    }
+                    consumer_sync();
+                    if (tr) trace_mark(p, l * 10 + 3);
                 }
-                consumer_sync();
-                if (tr) trace_mark(p, l * 10 + 3);
+                continue;
             }
-            // ---- P3: o_proj rows + residual (input: attention output o)
-            if (P.x1 > P.x0) {
-                prep_input<NI>(S, p, p.ll_o, nullptr, HQD, tag(l, PH_O), nullptr, xr, par);
-                if (tr) trace_mark(p, l * 10 + 4);
-                const uint32_t t = tag(l, PH_X1);
-                phase_any<false>(ring, S, p, P.x1 - P.x0, P.rps_o, HQD, xr, [&](int i, float v) {
-                    const float nx = S.xown[i] + v;
-                    S.xown[i] = nx;
-                    ll_store(p.ll_x + P.x0 + i, t, nx);
-                });
-                if (tr) trace_mark(p, l * 10 + 5);
+            // ---- a matrix phase: input vector (RMS-normalised where a gain is given) -> rows
+            const unsigned long long* in_ll = p.ll_x;
+            const bf16_t* in_row = nullptr;
+            const bf16_t* gain = nullptr;
+            int n_in = p.H, rows, per, K = p.H, group = 8;
+            uint32_t in_tag = 0;
+            bool glu = false;
+            PhaseOut o{EMIT_LL, nullptr, 0u, nullptr, 0};
+            if (e == 0) {          // QKV rows, input rms_norm(x) * g_in
+                in_row = l == 0 ? erow : nullptr;
+                in_tag = l == 0 ? 0u : tag(l - 1, PH_X2);
+                gain = Lw->g_in;
+                rows = P.q1 - P.q0; per = P.rps_h;
+                o.ll = p.ll_qkv + P.q0; o.tag = tag(l, PH_QKV);
+            } else if (e == 2) {   // o_proj rows + residual, input: attention output
+                in_ll = p.ll_o; n_in = HQD; in_tag = tag(l, PH_O);
+                rows = P.x1 - P.x0; per = P.rps_o; K = HQD;
+                o.kind = EMIT_RESID; o.ll = p.ll_x + P.x0; o.tag = tag(l, PH_X1);
+            } else if (e == 3) {   // gate_up pairs + SwiGLU, input rms_norm(x) * g_post
+                in_tag = tag(l, PH_X1); gain = Lw->g_post;
+                rows = P.f1 - P.f0; per = P.pps_gu; glu = true;
+                o.ll = p.ll_h + P.f0; o.tag = tag(l, PH_H);
+            } else if (e == 4) {   // down_proj rows + residual, input: h
+                in_ll = p.ll_h; n_in = p.F; in_tag = tag(l, PH_H);
+                rows = P.x1 - P.x0; per = P.rps_f; K = p.F;
+                o.kind = EMIT_RESID; o.ll = p.ll_x + P.x0; o.tag = tag(l, PH_X2);
+            } else {               // tied lm_head rows + argmax, input rms_norm(x) * final_norm
+                in_tag = tag(p.NL - 1, PH_X2); gain = p.final_norm;
+                rows = P.v1 - P.v0; per = P.rps_h; group = 3;   // bandwidth-bound: hand slots back sooner
+                o.kind = EMIT_LOGITS; o.logits = p.logits + P.v0; o.row0 = P.v0;
             }
-            // ---- P4: gate_up pairs + SwiGLU (input: rms_norm(x) * g_post) -> tagged h
-            if (P.f1 > P.f0) {
-                prep_input<NI>(S, p, p.ll_x, nullptr, p.H, tag(l, PH_X1), Lw.g_post, xr, par);
-                if (tr) trace_mark(p, l * 10 + 6);
-                const uint32_t t = tag(l, PH_H);
-                unsigned long long* dst = p.ll_h + P.f0;
-                phase_any<true>(ring, S, p, P.f1 - P.f0, P.pps_gu, p.H, xr,
-                                [&](int i, float v) { ll_store(dst + i, t, v); });
-                if (tr) trace_mark(p, l * 10 + 7);
+            if (rows > 0) {
+                const float r = prep_input(S, p, in_ll, in_row, n_in, in_tag, gain, xs, par);
+                if (tr) trace_mark(p, e == PH_PER_LAYER ? 10 * p.NL + 1 : l * 10 + 2 * e);
+                gemv_phase(ring, S, p, glu, rows, per, K, xs, r, group, o, best, besti, kpar);
+                if (tr && e != PH_PER_LAYER) trace_mark(p, l * 10 + 2 * e + 1);
             }
-            // ---- P5: down_proj rows + residual (input: h)
-            if (P.x1 > P.x0) {
-                prep_input<NI>(S, p, p.ll_h, nullptr, p.F, tag(l, PH_H), nullptr, xr, par);
-                if (tr) trace_mark(p, l * 10 + 8);
-                const uint32_t t = tag(l, PH_X2);
-                phase_any<false>(ring, S, p, P.x1 - P.x0, P.rps_f, p.F, xr, [&](int i, float v) {
-                    const float nx = S.xown[i] + v;
-                    S.xown[i] = nx;
-                    ll_store(p.ll_x + P.x0 + i, t, nx);
-                });
-                if (tr) trace_mark(p, l * 10 + 9);
-            }
-        }
-        // ---- final RMSNorm + tied lm_head + argmax
-        float best = -INFINITY;
-        int besti = 0x7fffffff;
-        if (P.v1 > P.v0) {
-            prep_input<NI>(S, p, p.ll_x, nullptr, p.H, tag(p.NL - 1, PH_X2), p.final_norm, xr, par);
-            if (tr) trace_mark(p, 10 * p.NL + 1);
-            phase_any<false>(ring, S, p, P.v1 - P.v0, P.rps_h, p.H, xr, [&](int i, float v) {
-                const int row = P.v0 + i;
-                p.logits[row] = v;
-                if (am_better(v, row, best, besti)) {
-                    best = v;
-                    besti = row;
-                }
-            }, 3);
         }
         if (tr) trace_mark(p, 10 * p.NL + 2);
-        // lane 0 of each warp holds its best; reduce over the CTA, then over the grid
+        // each thread holds the best of the logits it emitted: reduce over the warp, the CTA, then the grid
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, besti, o);
+            if (am_better(ov, oi, best, besti)) {
+                best = ov;
+                besti = oi;
+            }
+        }
         float* bv = S.red + 16;
         int* bi = reinterpret_cast<int*>(S.red + 32);
         if (lane == 0) {
@@ -931,20 +1066,13 @@ __global__ void __launch_bounds__(NT, 1) decode_persistent_kernel(const DecodePa
 
 using KernelFn = void (*)(const DecodeParams);
 
-KernelFn pick_kernel(int D, int G, int ni) {
-    if (ni <= 4) {
-        if (D == 32 && G == 2) return decode_persistent_kernel<32, 2, 4>;
-        if (D == 64 && G == 2) return decode_persistent_kernel<64, 2, 4>;
-        if (D == 128 && G == 2) return decode_persistent_kernel<128, 2, 4>;
-    }
-    if (ni <= 12) {
-        if (D == 128 && G == 1) return decode_persistent_kernel<128, 1, 12>;
-        if (D == 128 && G == 2) return decode_persistent_kernel<128, 2, 12>;
-        if (D == 128 && G == 4) return decode_persistent_kernel<128, 4, 12>;
-        if (D == 128 && G == 8) return decode_persistent_kernel<128, 8, 12>;
-        if (D == 64 && G == 2) return decode_persistent_kernel<64, 2, 12>;
-        if (D == 32 && G == 2) return decode_persistent_kernel<32, 2, 12>;
-    }
+KernelFn pick_kernel(int D, int G) {
+    if (D == 128 && G == 1) return decode_persistent_kernel<128, 1>;
+    if (D == 128 && G == 2) return decode_persistent_kernel<128, 2>;
+    if (D == 128 && G == 4) return decode_persistent_kernel<128, 4>;
+    if (D == 128 && G == 8) return decode_persistent_kernel<128, 8>;
+    if (D == 64 && G == 2) return decode_persistent_kernel<64, 2>;
+    if (D == 32 && G == 2) return decode_persistent_kernel<32, 2>;
     return nullptr;
 }
 
@@ -954,9 +1082,10 @@ cudaError_t decode_persistent_plan(const Shape& sh, int device, DecodeLaunch* ou
     *out = DecodeLaunch{};
     const int G = sh.HQ / sh.HKV;
     const int kmax_in = sh.H > sh.HQ * sh.D ? (sh.H > sh.F ? sh.H : sh.F) : (sh.HQ * sh.D > sh.F ? sh.HQ * sh.D : sh.F);
-    const int ni = (kmax_in + 255) / 256;
-    KernelFn fn = pick_kernel(sh.D, G, ni);
+    KernelFn fn = pick_kernel(sh.D, G);
     if (!fn) return cudaErrorNotSupported;
+    // a tagged vector is fetched by at most MAX_PR pairs per consumer thread
+    if (kmax_in > 2 * MAX_PR * NCT || (G + 2) * sh.D > 2 * MAX_PR * NCT) return cudaErrorNotSupported;
     // every matrix row and every GU pair must fit one ring slot
     if ((size_t)sh.H * 4 > SLOT || (size_t)sh.HQ * sh.D * 2 > SLOT || (size_t)sh.F * 2 > SLOT) return cudaErrorNotSupported;
     int sms = 0, max_smem = 0, coop = 0;
