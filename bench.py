@@ -68,6 +68,13 @@ def workload_desc(wl):
             "batch": wl.batch, "l2": "inputs larger than L2 (1.19 GB of bf16 weights per step), no flush"}
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the decode
+# kernel, from the ncu capture summarised in profiles/decode_persistent_funasr_nano_short.md
+# (11th decode step of funasr_nano_short).  Reported only for that workload; it must be
+# re-captured (or dropped) whenever the kernel changes.
+PROFILED_DECODE_TRAFFIC = {"funasr_nano_short": 1_204_227_328}
+
+
 def decode_step_bytes(shape, L):
     """Algorithmic HBM bytes of one batch-1 decode step whose KV length after the
     append is L: every weight once (embedding row only for the gather; the full
@@ -312,9 +319,12 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded random-init bf16 weights of the Qwen3-0.6B shape; seeded ids and audio rows)",
             "config": dict(workload_desc(wl), parallelism=f"replicas{world}"),
-            "roofline": {"bound": "hbm", "kernel": "decode step (all kernels of one token)",
+            "roofline": {"bound": "hbm",
+                         "kernel": ("decode_persistent_kernel (one launch per token)" if dec.decode_kernel == 0
+                                    else "decode step (graph of the CUDA-core kernels of one token)"),
                          "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                         "peak_kind": peak_kind, "traffic": None,
+                         "peak_kind": peak_kind,
+                         "traffic": (PROFILED_DECODE_TRAFFIC.get(wl.name) if dec.decode_kernel == 0 else None),
                          "algorithmic_bytes_per_launch": bytes_per_token},
             "clocks": clocks, "gpu_launches": int(launches) * world,
             "e2e": e2e}
