@@ -85,6 +85,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 2^x with the MUFU instruction (relative error about 2^-22, far below P's bf16 rounding);
+// -inf gives +0.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 // K-major operand, 128-byte swizzle: 128-byte rows, 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t desc_kmajor(const void* p) {
     uint64_t d = (uint64_t)((s32(p) >> 4) & 0x3FFFu);
@@ -246,22 +253,29 @@ __global__ void __launch_bounds__(192, 1) attn_prefill_tc_kernel(const __grid_co
         };
         for (int j = 0; j < nt; ++j) {
             const int st = j & 1;
+            // a tile wholly below the diagonal (every key visible to every row) needs no mask
+            const bool full = (j * KT + KT - 1 <= pos0 + q0) && (j * KT + KT <= L);
             mb_wait(&B->s_full[st], (j >> 1) & 1, 20);
             tc_fence_after();
             const uint32_t sadr = tmem + lane_off + st * 128;
-            float mx = -INFINITY;
+            float mx = -INFINITY;   // max raw score (scale_log2 > 0 commutes with the max)
 #pragma unroll
             for (int c = 0; c < KT / 32; ++c) {
                 float sv[32];
                 tmem_ld32(sadr + 32 * c, sv);
+                if (full) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const int key = j * KT + 32 * c + k;
-                    if (key <= qpos && key < L) mx = fmaxf(mx, sv[k] * scale_log2);
+                    for (int k = 0; k < 32; ++k) mx = fmaxf(mx, sv[k]);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        const int key = j * KT + 32 * c + k;
+                        if (key <= qpos && key < L) mx = fmaxf(mx, sv[k]);
+                    }
                 }
             }
-            const float m_new = fmaxf(m, mx);
-            const float corr = (m == -INFINITY) ? 0.f : exp2f(m - m_new);
+            const float m_new = fmaxf(m, mx * scale_log2);
+            const float corr = (m == -INFINITY) ? 0.f : ex2(m - m_new);
             // P_j into the swizzled K-major block layout the MMA reads (rows 128 B, 16-byte
             // chunk c of row r at chunk position c ^ (r & 7))
             mb_wait(&B->p_free[st], ((j >> 1) & 1) ^ 1, 21);
@@ -272,12 +286,20 @@ __global__ void __launch_bounds__(192, 1) attn_prefill_tc_kernel(const __grid_co
                 float sv[32];
                 tmem_ld32(sadr + 32 * c, sv);
                 float pv[32];
+                if (full) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const int key = j * KT + 32 * c + k;
-                    const bool vis = key <= qpos && key < L && m_new != -INFINITY;
-                    pv[k] = vis ? exp2f(sv[k] * scale_log2 - m_new) : 0.f;
-                    lsum += pv[k];
+                    for (int k = 0; k < 32; ++k) {
+                        pv[k] = ex2(fmaf(sv[k], scale_log2, -m_new));
+                        lsum += pv[k];
+                    }
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        const int key = j * KT + 32 * c + k;
+                        const bool vis = key <= qpos && key < L && m_new != -INFINITY;
+                        pv[k] = vis ? ex2(fmaf(sv[k], scale_log2, -m_new)) : 0.f;
+                        lsum += pv[k];
+                    }
                 }
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {   // four 16-byte chunks of 8 keys
