@@ -86,12 +86,31 @@ struct BatchWork {
     float *X = nullptr, *qkv = nullptr, *q = nullptr, *part_ml = nullptr, *part_o = nullptr, *gu = nullptr,
           *logits = nullptr;
     bf16_t *Xn = nullptr, *attn = nullptr, *h = nullptr;
+    int* h_tokens = nullptr;             // pinned staging of the step's tokens, two buffers of cap
+    cudaEvent_t tok_ev[2] = {nullptr, nullptr};   // each buffer's upload
+    int tok_slot = 0;
     int n_split = 1;
+    // The step's kernels as a CUDA graph for the current composition: the first step of a
+    // composition runs eagerly, the second is captured, later ones replay it.
+    cudaGraphExec_t exec = nullptr;
+    uint64_t graph_kernels = 0;
+    int steps_same = 0;                  // steps run since the composition last changed
+    int graph_impl = -1;                 // GEMM implementation the graph was captured with
+    void drop_graph() {
+        if (exec) cudaGraphExecDestroy(exec);
+        exec = nullptr;
+        graph_kernels = 0;
+        steps_same = 0;
+    }
     void release() {
+        drop_graph();
         void* ps[] = {d_streams, d_tokens, d_am, X, qkv, q, part_ml, part_o, gu, logits, Xn, attn, h};
         for (void* p : ps)
             if (p) cudaFree(p);
         if (h_am) cudaFreeHost(h_am);
+        if (h_tokens) cudaFreeHost(h_tokens);
+        for (cudaEvent_t e : tok_ev)
+            if (e) cudaEventDestroy(e);
         *this = BatchWork();
     }
 };
@@ -502,6 +521,8 @@ int ensure_batch_work(qdec_ctx* const* ctxs, int n) {
         CK(dalloc(&b.d_tokens, (size_t)n));
         CK(dalloc(&b.d_am, (size_t)n));
         CK(cudaMallocHost(reinterpret_cast<void**>(&b.h_am), (size_t)n * sizeof(int)));
+        CK(cudaMallocHost(reinterpret_cast<void**>(&b.h_tokens), (size_t)2 * n * sizeof(int)));
+        for (cudaEvent_t& e : b.tok_ev) CK(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
         CK(dalloc(&b.X, (size_t)n * sh.H));
         CK(dalloc(&b.Xn, (size_t)n * sh.H));
         CK(dalloc(&b.qkv, (size_t)n * sh.qkv_rows()));
@@ -517,6 +538,7 @@ int ensure_batch_work(qdec_ctx* const* ctxs, int n) {
     bool same = (int)b.members.size() == n;
     for (int i = 0; same && i < n; ++i) same = b.members[i] == ctxs[i];
     if (!same) {
+        b.drop_graph();
         std::vector<BatchStream> hs(n);
         b.members.assign(ctxs, ctxs + n);
         for (int i = 0; i < n; ++i)
@@ -544,6 +566,56 @@ int batch_gemm(qdec_ctx* c, const bf16_t* A, int lda, const bf16_t* W, int M, in
     return QDEC_OK;
 }
 
+// The kernels of one lockstep step, reading d_tokens and writing b.logits and d_am; returns
+// the number of kernels launched through *kernels.
+int batch_body(qdec_ctx* c0, int n, cudaStream_t s, uint64_t* kernels) {
+    const Shape& sh = c0->sh;
+    BatchWork& b = *c0->batch;
+    int rc;
+    CK(launch_batch_embed(c0->embed, sh.H, b.d_tokens, b.d_streams, n, b.X, s));
+    const int qd = sh.HQ * sh.D;
+    uint64_t k = 1;
+    for (int l = 0; l < sh.NL; ++l) {
+        const LayerW& w = c0->layers[l];
+        CK(launch_rmsnorm_bf16(b.X, n, sh.H, w.g_in, sh.eps, b.Xn, s));
+        if ((rc = batch_gemm(c0, b.Xn, sh.H, w.wqkv, n, sh.qkv_rows(), sh.H, false, b.qkv, sh.qkv_rows(), s))) return rc;
+        CK(launch_batch_qk_rope(b.qkv, sh, l, w.g_q, w.g_k, b.d_streams, n, b.q, s));
+        CK(launch_batch_attention(b.q, sh, l, b.d_streams, n, b.n_split, b.part_ml, b.part_o, b.attn, s));
+        if ((rc = batch_gemm(c0, b.attn, qd, w.wo, n, sh.H, qd, true, b.X, sh.H, s))) return rc;
+        CK(launch_rmsnorm_bf16(b.X, n, sh.H, w.g_post, sh.eps, b.Xn, s));
+        if ((rc = batch_gemm(c0, b.Xn, sh.H, w.wgu, n, 2 * sh.F, sh.H, false, b.gu, 2 * sh.F, s))) return rc;
+        CK(launch_batch_swiglu(b.gu, sh.F, n, b.h, s));
+        if ((rc = batch_gemm(c0, b.h, sh.F, w.wd, n, sh.H, sh.F, true, b.X, sh.H, s))) return rc;
+        k += 10;
+    }
+    CK(launch_rmsnorm_bf16(b.X, n, sh.H, c0->final_norm, sh.eps, b.Xn, s));
+    if ((rc = batch_gemm(c0, b.Xn, sh.H, c0->embed, n, sh.V, sh.H, false, b.logits, sh.V, s))) return rc;
+    CK(launch_batch_argmax(b.logits, sh.V, sh.V, b.d_streams, n, b.d_am, s));
+    *kernels = k + 3;
+    return QDEC_OK;
+}
+
+// Captures batch_body into b.exec on the context's capture stream.
+int capture_batch(qdec_ctx* c0, int n) {
+    BatchWork& b = *c0->batch;
+    cudaGraph_t g = nullptr;
+    uint64_t kernels = 0;
+    CK(cudaStreamBeginCapture(c0->cap_stream, cudaStreamCaptureModeThreadLocal));
+    int rc = batch_body(c0, n, c0->cap_stream, &kernels);
+    cudaError_t e = cudaStreamEndCapture(c0->cap_stream, &g);
+    if (rc != QDEC_OK) {
+        if (g) cudaGraphDestroy(g);
+        return rc;
+    }
+    CK(e);
+    e = cudaGraphInstantiate(&b.exec, g, 0);
+    cudaGraphDestroy(g);
+    CK(e);
+    b.graph_kernels = kernels;
+    b.graph_impl = c0->prefill_gemm;
+    return QDEC_OK;
+}
+
 int batch_step(qdec_ctx* const* ctxs, int n, const int32_t* tokens, float* logits_out, int32_t* argmax_out) {
     qdec_ctx* c0 = ctxs[0];
     const Shape& sh = c0->sh;
@@ -561,31 +633,30 @@ int batch_step(qdec_ctx* const* ctxs, int n, const int32_t* tokens, float* logit
     int rc = ensure_batch_work(ctxs, n);
     if (rc != QDEC_OK) return rc;
     BatchWork& b = *c0->batch;
-    CK(cudaMemcpyAsync(b.d_tokens, tokens, (size_t)n * sizeof(int), cudaMemcpyHostToDevice, s));
-    CK(launch_batch_embed(c0->embed, sh.H, b.d_tokens, b.d_streams, n, b.X, s));
-    const int qd = sh.HQ * sh.D;
-    uint64_t kernels = 1;
-    for (int l = 0; l < sh.NL; ++l) {
-        const LayerW& w = c0->layers[l];
-        CK(launch_rmsnorm_bf16(b.X, n, sh.H, w.g_in, sh.eps, b.Xn, s));
-        if ((rc = batch_gemm(c0, b.Xn, sh.H, w.wqkv, n, sh.qkv_rows(), sh.H, false, b.qkv, sh.qkv_rows(), s))) return rc;
-        CK(launch_batch_qk_rope(b.qkv, sh, l, w.g_q, w.g_k, b.d_streams, n, b.q, s));
-        CK(launch_batch_attention(b.q, sh, l, b.d_streams, n, b.n_split, b.part_ml, b.part_o, b.attn, s));
-        if ((rc = batch_gemm(c0, b.attn, qd, w.wo, n, sh.H, qd, true, b.X, sh.H, s))) return rc;
-        CK(launch_rmsnorm_bf16(b.X, n, sh.H, w.g_post, sh.eps, b.Xn, s));
-        if ((rc = batch_gemm(c0, b.Xn, sh.H, w.wgu, n, 2 * sh.F, sh.H, false, b.gu, 2 * sh.F, s))) return rc;
-        CK(launch_batch_swiglu(b.gu, sh.F, n, b.h, s));
-        if ((rc = batch_gemm(c0, b.h, sh.F, w.wd, n, sh.H, sh.F, true, b.X, sh.H, s))) return rc;
-        kernels += 12;
+    if (b.exec && b.graph_impl != c0->prefill_gemm) b.drop_graph();
+    // two pinned staging buffers: wait only for the upload that last used this one
+    int* ht = b.h_tokens + (size_t)b.tok_slot * b.cap;
+    CK(cudaEventSynchronize(b.tok_ev[b.tok_slot]));
+    memcpy(ht, tokens, (size_t)n * sizeof(int));
+    CK(cudaMemcpyAsync(b.d_tokens, ht, (size_t)n * sizeof(int), cudaMemcpyHostToDevice, s));
+    CK(cudaEventRecord(b.tok_ev[b.tok_slot], s));
+    b.tok_slot ^= 1;
+    if (!b.exec && b.steps_same >= 1) {
+        rc = capture_batch(c0, n);
+        if (rc != QDEC_OK) return rc;
     }
-    CK(launch_rmsnorm_bf16(b.X, n, sh.H, c0->final_norm, sh.eps, b.Xn, s));
-    float* lg = (logits_out && is_device_ptr(logits_out) && aligned16(logits_out)) ? logits_out : b.logits;
-    if ((rc = batch_gemm(c0, b.Xn, sh.H, c0->embed, n, sh.V, sh.H, false, lg, sh.V, s))) return rc;
-    CK(launch_batch_argmax(lg, sh.V, sh.V, b.d_streams, n, b.d_am, s));
-    count_launches(kernels + 3);
+    if (b.exec) {
+        CK(cudaGraphLaunch(b.exec, s));
+        count_launches(b.graph_kernels);
+    } else {
+        uint64_t kernels = 0;
+        if ((rc = batch_body(c0, n, s, &kernels))) return rc;
+        count_launches(kernels);
+    }
+    ++b.steps_same;
     for (int i = 0; i < n; ++i) ctxs[i]->position += 1;
-    if (logits_out && lg != logits_out)
-        CK(cudaMemcpyAsync(logits_out, lg, (size_t)n * sh.V * sizeof(float), cudaMemcpyDefault, s));
+    if (logits_out)
+        CK(cudaMemcpyAsync(logits_out, b.logits, (size_t)n * sh.V * sizeof(float), cudaMemcpyDefault, s));
     for (cudaEvent_t e : evs) {   // the other streams wait for the batch before their next work
         CK(cudaEventRecord(e, s));
     }

@@ -77,9 +77,34 @@ __global__ void batch_qk_rope_kernel(const float* __restrict__ qkv, int HQ, int 
 }
 
 constexpr int BNT = 128, BWARPS = BNT / 32;
+constexpr int BP = 8;   // key positions a warp loads and scores together
+
+// 2^x with the MUFU instruction (relative error about 2^-22); -inf gives +0.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// The EPL bf16 values of lane `lane` in a D-wide row, widened to fp32.
+template <int EPL>
+__device__ __forceinline__ void row_lane(const bf16_t* row, int lane, float (&out)[EPL]) {
+    if constexpr (EPL == 4) {
+        const uint2 w = *reinterpret_cast<const uint2*>(row + lane * 4);
+        out[0] = bf_lo(w.x); out[1] = bf_hi(w.x); out[2] = bf_lo(w.y); out[3] = bf_hi(w.y);
+    } else if constexpr (EPL == 2) {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(row + lane * 2);
+        out[0] = bf_lo(w); out[1] = bf_hi(w);
+    } else {
+        out[0] = bf1(row[lane]);
+    }
+}
 
 // Split-KV attention of one stream's kv head over its keys [0, pos + 1).
-// grid (HKV, n_split, n); partials [n][HQ][n_split] (m, l) and (o[D]).
+// grid (HKV, n_split, n); partials [n][HQ][n_split] (m, l) and (o[D]), m in log2 units.
+// Each warp takes groups of BP positions: their K/V loads are all in flight together, the
+// BP x G scores are reduced across the warp together, then one online-softmax update
+// (exp2 of scores pre-scaled by log2(e)/sqrt(D)) folds the group in.
 template <int D, int G>
 __global__ void __launch_bounds__(BNT) batch_attn_kernel(const float* __restrict__ q, int HQ, int HKV, int layer,
                                                          const BatchStream* __restrict__ bs, int n_split,
@@ -97,7 +122,7 @@ __global__ void __launch_bounds__(BNT) batch_attn_kernel(const float* __restrict
     const size_t layer_stride = (size_t)2 * HKV * st.max_seq * D;
     const bf16_t* kb = st.kv + (size_t)layer * layer_stride + (size_t)gk * st.max_seq * D;
     const bf16_t* vb = kb + (size_t)HKV * st.max_seq * D;
-    const float scale = rsqrtf((float)D);
+    const float scale = rsqrtf((float)D) * 1.4426950408889634f;   // scores in log2 units
     float qv[G][EPL], m[G], l[G], o[G][EPL];
 #pragma unroll
     for (int gi = 0; gi < G; ++gi) {
@@ -109,25 +134,49 @@ __global__ void __launch_bounds__(BNT) batch_attn_kernel(const float* __restrict
         m[gi] = -INFINITY;
         l[gi] = 0.f;
     }
-    for (int j = j0 + warp; j < j1; j += BWARPS) {
-        float kf[EPL], vf[EPL];
+    for (int jb = j0 + warp * BP; jb < j1; jb += BWARPS * BP) {
+        float kf[BP][EPL], vf[BP][EPL];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-            kf[e] = bf1(kb[(size_t)j * D + lane * EPL + e]);
-            vf[e] = bf1(vb[(size_t)j * D + lane * EPL + e]);
+        for (int p = 0; p < BP; ++p) {
+            const int jj = min(jb + p, j1 - 1);   // past the end: a valid row, weighted 0 below
+            row_lane<EPL>(kb + (size_t)jj * D, lane, kf[p]);
+            row_lane<EPL>(vb + (size_t)jj * D, lane, vf[p]);
         }
+        float sc[BP][G];
+#pragma unroll
+        for (int p = 0; p < BP; ++p)
+#pragma unroll
+            for (int gi = 0; gi < G; ++gi) {
+                float d0 = 0.f;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) d0 = fmaf(qv[gi][e], kf[p][e], d0);
+                sc[p][gi] = d0;
+            }
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1)
+#pragma unroll
+            for (int p = 0; p < BP; ++p)
+#pragma unroll
+                for (int gi = 0; gi < G; ++gi) sc[p][gi] += __shfl_xor_sync(0xffffffffu, sc[p][gi], sh);
 #pragma unroll
         for (int gi = 0; gi < G; ++gi) {
-            float d0 = 0.f;
+            float mx = -INFINITY;
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) d0 = fmaf(qv[gi][e], kf[e], d0);
-            const float sc = warp_sum(d0);
-            const float mn = fmaxf(m[gi], sc);
-            const float corr = expf(m[gi] - mn);
-            const float pr = expf(sc - mn);
-            l[gi] = l[gi] * corr + pr;
+            for (int p = 0; p < BP; ++p)
+                if (jb + p < j1) mx = fmaxf(mx, sc[p][gi]);
+            const float mn = fmaxf(m[gi], mx);   // finite: position jb is always valid
+            const float corr = ex2(m[gi] - mn);  // 0 while m is -inf
+            float psum = 0.f;
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) o[gi][e] = fmaf(pr, vf[e], o[gi][e] * corr);
+            for (int e = 0; e < EPL; ++e) o[gi][e] *= corr;
+#pragma unroll
+            for (int p = 0; p < BP; ++p) {
+                const float pr = (jb + p < j1) ? ex2(sc[p][gi] - mn) : 0.f;
+                psum += pr;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) o[gi][e] = fmaf(pr, vf[p][e], o[gi][e]);
+            }
+            l[gi] = l[gi] * corr + psum;
             m[gi] = mn;
         }
     }
@@ -150,7 +199,7 @@ __global__ void __launch_bounds__(BNT) batch_attn_kernel(const float* __restrict
         if (M != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < BWARPS; ++w) {
-                const float f = expf(sm[w][gi] - M);
+                const float f = ex2(sm[w][gi] - M);
                 lt += f * sl[w][gi];
                 ot += f * so[w][gi][d];
             }
@@ -176,7 +225,7 @@ __global__ void batch_attn_merge_kernel(int HQ, int D, int n_split, const float*
         for (int k = 0; k < n_split; ++k) {
             const float mk = part_ml[(base + k) * 2];
             if (mk == -INFINITY) continue;
-            const float f = expf(mk - M);
+            const float f = ex2(mk - M);
             lt += f * part_ml[(base + k) * 2 + 1];
             ot += f * part_o[(base + k) * D + d];
         }
@@ -185,10 +234,15 @@ __global__ void batch_attn_merge_kernel(int HQ, int D, int n_split, const float*
 }
 
 // h = silu(gate) * up from the fp32 [n, 2F] projection (gate columns first), bf16 [n, F].
-__global__ void batch_swiglu_kernel(const float* __restrict__ gu, int F, bf16_t* __restrict__ h) {
-    const int s = blockIdx.x;
-    for (int j = threadIdx.x; j < F; j += blockDim.x)
-        h[(size_t)s * F + j] = f2bf(silu(gu[(size_t)s * 2 * F + j]) * gu[(size_t)s * 2 * F + F + j]);
+// One thread per pair of columns (F even) over all n rows.
+__global__ void batch_swiglu_kernel(const float* __restrict__ gu, int F, int n, bf16_t* __restrict__ h) {
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;   // pair index
+    const int half = F >> 1;
+    if (idx >= n * half) return;
+    const int s = idx / half, j = 2 * (idx - s * half);
+    const float2 g = *reinterpret_cast<const float2*>(gu + (size_t)s * 2 * F + j);
+    const float2 u = *reinterpret_cast<const float2*>(gu + (size_t)s * 2 * F + F + j);
+    *reinterpret_cast<uint32_t*>(h + (size_t)s * F + j) = pack_bf2(silu(g.x) * u.x, silu(g.y) * u.y);
 }
 
 // Argmax of each logits row (lowest index on ties), into the stream's argmax and out[s];
@@ -284,7 +338,9 @@ cudaError_t launch_batch_attention(const float* q, const Shape& sh, int layer, c
 
 cudaError_t launch_batch_swiglu(const float* gu, int F, int n, bf16_t* h, cudaStream_t st) {
     (void)cudaGetLastError();
-    batch_swiglu_kernel<<<n, 256, 0, st>>>(gu, F, h);
+    if (F % 2 != 0) return cudaErrorInvalidValue;
+    const int pairs = n * (F / 2);
+    batch_swiglu_kernel<<<(pairs + 255) / 256, 256, 0, st>>>(gu, F, n, h);
     return cudaGetLastError();
 }
 

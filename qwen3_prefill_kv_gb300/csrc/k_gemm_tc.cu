@@ -315,7 +315,8 @@ cudaError_t launch_gemm_tc(const bf16_t* A, int lda, const bf16_t* W, int M, int
         case GEMM_ADD_F32: return launch_bn<128, GEMM_ADD_F32, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
         case GEMM_SWIGLU_BF16: return launch_bn<128, GEMM_SWIGLU_BF16, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
         case GEMM_STORE_BF16: return launch_bn<128, GEMM_STORE_BF16, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
-        case GEMM_ATOMIC_F32: return launch_bn<128, GEMM_ATOMIC_F32, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
+        // split-K CTAs run few k-blocks each: a 3-stage ring (97 KB) lets two share an SM
+        case GEMM_ATOMIC_F32: return launch_bn<128, GEMM_ATOMIC_F32, 3>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from qwen3_prefill_kv_gb300 import synth
+from qwen3_prefill_kv_gb300 import synth, _lib
 from qwen3_prefill_kv_gb300._lib import Decoder, QdecError, DECODE_PERSISTENT, DECODE_GRAPH
 
 import _harness as H
@@ -204,6 +204,44 @@ def test_batch_step_matches_single_streams(model):
                                        atol=1e-2 * float(ls.abs().max()))
         toks = am                                    # greedy continuation per stream
     assert all(b.position == p.ids.numel() + 4 for b in branches)
+
+
+def test_batch_graph_follows_composition_and_options(model):
+    """The lockstep step is replayed from a graph after its first step; a new batch
+    composition or a GEMM-implementation change must rebuild it, with the argmax fed back
+    on the device (token -1) throughout."""
+    w, wd, orc = model
+    p = _prompt(12, 8, 12)
+    src = Decoder(SH, wd, max_seq=48)
+    src.prefill(p.ids, p.audio.cuda(), p.audio_offset)
+    A = [src.clone() for _ in range(3)]
+    S = [src.clone() for _ in range(3)]
+    first = synth.make_tokens(SH.vocab, 3, seed=5).numpy()
+    lb = torch.empty(3, SH.vocab, device="cuda")
+    ls = torch.empty(SH.vocab, device="cuda")
+
+    def check(batch, singles, toks, single_toks, k):
+        # the batch feeds its own argmax back on the device (token -1); the single streams get
+        # the batch's previous picks explicitly, so near ties cannot make the two diverge
+        am = Decoder.decode_step_batch(batch, toks, logits=lb[:len(batch)])
+        for i, sd in enumerate(singles):
+            sd.decode_step(int(single_toks[i]), logits=ls)
+            np.testing.assert_allclose(lb[i].cpu().numpy(), ls.cpu().numpy(), rtol=0,
+                                       atol=1e-2 * float(ls.abs().max()), err_msg=f"step {k} stream {i}")
+            assert am[i] == int(torch.argmax(lb[i]))
+        return am
+
+    am = check(A, S, first, first, 0)
+    for k in range(1, 4):                                # eager, captured, replayed
+        am = check(A, S, np.full(3, -1, dtype=np.int32), am, k)
+    am2 = am[[0, 2]]
+    for k in range(4, 7):                                # new composition
+        am2 = check([A[0], A[2]], [S[0], S[2]], np.full(2, -1, dtype=np.int32), am2, k)
+    A[0].set_option(_lib.OPT_PREFILL_IMPL, _lib.PREFILL_SIMT)
+    for k in range(7, 9):                                # CUDA-core GEMMs
+        am2 = check([A[0], A[2]], [S[0], S[2]], np.full(2, -1, dtype=np.int32), am2, k)
+    assert A[0].position == A[2].position == p.ids.numel() + 9 and A[1].position == p.ids.numel() + 4
+    assert np.array_equal(A[0].read_history(), S[0].read_history())
 
 
 def test_errors_leave_context_unchanged(model):
