@@ -129,6 +129,14 @@ __device__ __forceinline__ void ll_load2(const unsigned long long* p, unsigned l
 }
 __device__ __forceinline__ int volatile_load(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
 
+// 2^x with the MUFU instruction (relative error about 2^-22); -inf gives +0.  The attention
+// units keep scores, maxima and partial maxima in log2 units (q is pre-scaled by log2 e).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Optional phase trace: globaltimer (ns) at slot `idx` of this CTA's row.
 __device__ __forceinline__ void trace_mark(const DecodeParams& p, int idx) {
     if (p.trace) {
@@ -788,7 +796,7 @@ __global__ void __launch_bounds__(NT, 1) decode_persistent_kernel(const DecodePa
                             Lw->vc[((size_t)g * p.max_seq + p.pos) * D + d] = f2bf(xa[(G + 1) * D + d]);
                         }
                     }
-                    const float scale = rsqrtf((float)D);
+                    const float scale = rsqrtf((float)D) * 1.4426950408889634f;   // scores in log2 units
                     float qv[G][EPL], m[G], lsum[G], o[G][EPL];
     #pragma unroll
                     for (int gi = 0; gi < G; ++gi) {
@@ -838,14 +846,14 @@ __global__ void __launch_bounds__(NT, 1) decode_persistent_kernel(const DecodePa
                             for (int k = 0; k < KPW; ++k) mx = fmaxf(mx, s[k][gi]);
                             const float mn = fmaxf(m[gi], mx);
                             if (mn != -INFINITY) {
-                                const float corr = expf(m[gi] - mn);   // 0 when m was -inf
+                                const float corr = ex2(m[gi] - mn);   // 0 when m was -inf
                                 lsum[gi] *= corr;
     #pragma unroll
                                 for (int e = 0; e < EPL; ++e) o[gi][e] *= corr;
                                 m[gi] = mn;
     #pragma unroll
                                 for (int k = 0; k < KPW; ++k) {
-                                    s[k][gi] = (s[k][gi] == -INFINITY) ? 0.f : expf(s[k][gi] - mn);
+                                    s[k][gi] = ex2(s[k][gi] - mn);   // masked scores (-inf) give 0
                                     lsum[gi] += s[k][gi];
                                 }
                             } else {
@@ -880,8 +888,8 @@ __global__ void __launch_bounds__(NT, 1) decode_persistent_kernel(const DecodePa
                             for (int e = 0; e < EPL; ++e) d0 = fmaf(qv[gi][e], kf[e], d0);
                             const float sc = warp_sum(d0);
                             const float mn = fmaxf(m[gi], sc);
-                            const float corr = expf(m[gi] - mn);
-                            const float pr = expf(sc - mn);
+                            const float corr = ex2(m[gi] - mn);
+                            const float pr = ex2(sc - mn);
                             lsum[gi] = lsum[gi] * corr + pr;
     #pragma unroll
                             for (int e = 0; e < EPL; ++e) o[gi][e] = fmaf(pr, vf[e], o[gi][e] * corr);
@@ -911,7 +919,7 @@ __global__ void __launch_bounds__(NT, 1) decode_persistent_kernel(const DecodePa
     #pragma unroll
                         for (int w = 0; w < NCW; ++w) {
                             const float* a = S.att + ((size_t)w * G + gi) * (D + 2);
-                            const float f = (a[0] == -INFINITY) ? 0.f : expf(a[0] - M);
+                            const float f = (a[0] == -INFINITY) ? 0.f : ex2(a[0] - M);
                             lt += f * a[1];
                             ot += f * a[2 + d];
                         }
@@ -947,7 +955,7 @@ __global__ void __launch_bounds__(NT, 1) decode_persistent_kernel(const DecodePa
                                 for (int j = 0; j < p.n_chunks; ++j) {
                                     const float* a = base + (size_t)j * (D + 2);
                                     const float mj = __ldcg(a);
-                                    const float f = (mj == -INFINITY) ? 0.f : expf(mj - M);
+                                    const float f = (mj == -INFINITY) ? 0.f : ex2(mj - M);
                                     lt += f * __ldcg(a + 1);
                                     ot += f * __ldcg(a + 2 + d);
                                 }
