@@ -111,6 +111,27 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* b, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// True when all four barriers have completed the given phases.  One asm block, so the four
+// tests are in flight together (each result is needed only at the end).
+__device__ __forceinline__ bool mbar_test_wait4(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1, uint64_t* b2,
+                                                uint32_t p2, uint64_t* b3, uint32_t p3) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred q0, q1, q2, q3;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q3, [%7], %8;\n\t"
+        "and.pred q0, q0, q1;\n\t"
+        "and.pred q2, q2, q3;\n\t"
+        "and.pred q0, q0, q2;\n\t"
+        "selp.u32 %0, 1, 0, q0;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(b0)), "r"(p0), "r"(smem_u32(b1)), "r"(p1), "r"(smem_u32(b2)), "r"(p2), "r"(smem_u32(b3)),
+          "r"(p3)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      smem_u32(dst)),
@@ -414,6 +435,38 @@ struct Ring {
         wait(S, p, 0);
         return ptr(S, 0);
     }
+    // Waits for the stages 0 .. g-1 ahead (g < nslot): their barriers are tested four at a
+    // time in one go, and only an incomplete group falls back to the bounded per-stage waits.
+    __device__ void wait_group(const Ctx& S, const DecodeParams& p, int g) const {
+        for (int s0 = 0; s0 < g; s0 += 4) {
+            uint64_t* b[4];
+            uint32_t par[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                int s = slot + min(s0 + j, g - 1);
+                par[j] = parity;
+                if (s >= S.nslot) {
+                    s -= S.nslot;
+                    par[j] ^= 1u;
+                }
+                b[j] = &S.full[s];
+            }
+            if (!mbar_test_wait4(b[0], par[0], b[1], par[1], b[2], par[2], b[3], par[3]))
+                for (int j = s0; j < min(s0 + 4, g); ++j) wait(S, p, j);
+        }
+    }
+    // Hands back the next g stages (see release).
+    __device__ void release_group(const Ctx& S, int g) {
+        __syncwarp();
+        const bool give = (threadIdx.x & 31) == 0 && !reinterpret_cast<volatile int*>(S.flags)[F_ABORT];
+        for (int j = 0; j < g; ++j) {
+            if (give) mbar_arrive(&S.empty[slot]);
+            if (++slot == S.nslot) {
+                slot = 0;
+                parity ^= 1u;
+            }
+        }
+    }
     // After an abort a slot is never handed back: its copy may still be in flight, and the
     // producer must not reuse it (the final drain waits for it instead).
     __device__ void release(const Ctx& S) {
@@ -583,13 +636,13 @@ __device__ inline void gemv_phase(Ring& ring, const Ctx& S, const DecodeParams& 
     const float inv_per = 1.f / (float)per;
     for (int s0 = 0; s0 < nst; s0 += maxg) {
         const int g = min(maxg, nst - s0);
-        for (int s = 0; s < g; ++s) ring.wait(S, p, s);
+        ring.wait_group(S, p, g);
         const int r0 = s0 * per, r1 = min(rows, (s0 + g) * per);
         if (glu) group_rows<true, 3>(ring, S, s0, r0, r1, rows, per, inv_per, K, xs, r, out, best, besti);
         else if (r1 - r0 >= 3 * NCW) group_rows<false, 4>(ring, S, s0, r0, r1, rows, per, inv_per, K, xs, r, out, best, besti);
         else if (K >= 512 && r1 - r0 < 2 * NCW) ksplit_rows(ring, S, s0, r0, r1, per, inv_per, K, xs, r, out, best, besti, kpar);
         else group_rows<false, 1>(ring, S, s0, r0, r1, rows, per, inv_per, K, xs, r, out, best, besti);
-        for (int s = 0; s < g; ++s) ring.release(S);
+        ring.release_group(S, g);
     }
 }
 
