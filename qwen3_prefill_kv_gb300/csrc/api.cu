@@ -352,7 +352,7 @@ int copy_logits_out(qdec_ctx* c, float* dst) {
     return QDEC_OK;
 }
 
-constexpr uint64_t kPrefillKernelsPerLayer = 8;
+constexpr uint64_t kPrefillKernelsPerLayer = 7;   // + 1 when the QKV epilogue is not fused
 
 // Prefill GEMM: tcgen05 kernel where the shape allows it (and it is selected), else CUDA cores.
 cudaError_t prefill_gemm(const qdec_ctx* c, const bf16_t* A, int lda, const bf16_t* W, int M, int N, int K, int mode,
@@ -369,10 +369,17 @@ int prefill_layer(qdec_ctx* c, int l, int T) {
     cudaStream_t s = c->stream;
     const int qd = sh.HQ * sh.D;
     CK(launch_rmsnorm_bf16(c->p_X, T, sh.H, w.g_in, sh.eps, c->p_Xn, s));
-    CK(prefill_gemm(c, c->p_Xn, sh.H, w.wqkv, T, sh.qkv_rows(), sh.H, GEMM_STORE_F32, 0, c->p_qkv, nullptr,
+    if (c->prefill_gemm == QDEC_PREFILL_TCGEN05 && gemm_tc_qkv_rope_supported(sh, sh.H)) {
+        // QKV projection with the per-head norm, RoPE and KV append in its epilogue
+        QkvRopeEpi e{c->rope, w.g_q, w.g_k, c->p_Q, c->k_cache(l), c->v_cache(l), 0, sh.HQ, sh.HKV, sh.max_seq, sh.eps};
+        CK(launch_gemm_tc_qkv_rope(c->p_Xn, sh.H, w.wqkv, T, sh.H, e, s));
+    } else {
+        CK(prefill_gemm(c, c->p_Xn, sh.H, w.wqkv, T, sh.qkv_rows(), sh.H, GEMM_STORE_F32, 0, c->p_qkv, nullptr,
                         sh.qkv_rows(), s));
-    CK(launch_qk_norm_rope_append(c->p_qkv, T, sh, c->d_zero, w.g_q, w.g_k, c->rope, c->p_Q, nullptr,
-                                  c->k_cache(l), c->v_cache(l), s));
+        CK(launch_qk_norm_rope_append(c->p_qkv, T, sh, c->d_zero, w.g_q, w.g_k, c->rope, c->p_Q, nullptr,
+                                      c->k_cache(l), c->v_cache(l), s));
+        count_launches(1);
+    }
     if (c->prefill_gemm == QDEC_PREFILL_TCGEN05 && attention_tc_supported(sh))
         CK(launch_attention_prefill_tc(c->p_Q, T, sh, 0, c->k_cache(l), c->v_cache(l), c->p_O, s));
     else

@@ -65,7 +65,8 @@ int set_error(int code, const char* fmt, ...);
 cudaError_t launch_rmsnorm_bf16(const float* X, int T, int H, const bf16_t* g, float eps,
                                 bf16_t* out, cudaStream_t s);
 
-enum GemmMode { GEMM_STORE_F32 = 0, GEMM_ADD_F32 = 1, GEMM_SWIGLU_BF16 = 2, GEMM_STORE_BF16 = 3, GEMM_ATOMIC_F32 = 4 };
+enum GemmMode { GEMM_STORE_F32 = 0, GEMM_ADD_F32 = 1, GEMM_SWIGLU_BF16 = 2, GEMM_STORE_BF16 = 3, GEMM_ATOMIC_F32 = 4,
+                GEMM_QKV_ROPE = 5 };
 // C[M, N] (op) A[M, K] . W[N, K]^T.  SWIGLU: W is [2N, K] (gate rows, then up rows at
 // offset `up_off` rows) and C_bf16[m, n] = silu(gate) * up.
 cudaError_t launch_gemm_simt(const bf16_t* A, int lda, const bf16_t* W, int M, int N, int K, int mode,
@@ -77,6 +78,19 @@ bool gemm_tc_supported(int N, int K, int mode, int lda);
 // GEMM_ATOMIC_F32 (C += acc with fp32 vector atomics) may split K over `splits` CTAs per tile.
 cudaError_t launch_gemm_tc(const bf16_t* A, int lda, const bf16_t* W, int M, int N, int K, int mode, int up_off,
                            float* Cf, bf16_t* Cb, int ldc, cudaStream_t s, int splits = 1);
+// The packed QKV projection with the per-head epilogue fused (head_dim 128, one head per
+// 128-column tile): q heads -> RMSNorm(g_q) + NeoX RoPE at pos0 + row -> bf16 q [M][HQ][128];
+// k heads -> RMSNorm(g_k) + RoPE -> bf16 K cache slot pos0 + row; v heads -> bf16 V cache.
+struct QkvRopeEpi {
+    const float2* rope;        // [max_seq][64] (cos, sin)
+    const bf16_t *g_q, *g_k;   // [128]
+    bf16_t *q, *kc, *vc;       // q [M][HQ][128]; this layer's K and V cache [HKV][max_seq][128]
+    int pos0, HQ, HKV, max_seq;
+    float eps;
+};
+bool gemm_tc_qkv_rope_supported(const Shape& sh, int lda);
+cudaError_t launch_gemm_tc_qkv_rope(const bf16_t* A, int lda, const bf16_t* W, int M, int K, const QkvRopeEpi& epi,
+                                    cudaStream_t s);
 // First timeout code recorded by a tensor-core kernel since the last call (0 = none);
 // synchronous, clears the flag.
 int tc_error_read_and_clear();

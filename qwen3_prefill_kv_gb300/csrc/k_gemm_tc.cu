@@ -10,7 +10,10 @@
 //   warp 1   allocates BN TMEM columns and issues tcgen05.mma (M = 128, N = BN, K = 16) from
 //            one thread, committing each stage back to its empty barrier;
 //   warps 2-5 epilogue: tcgen05.ld of the accumulator (one TMEM lane = one output row),
-//            then store / residual add / SwiGLU to global memory.
+//            then store / residual add / SwiGLU / split-K atomics to global memory, or for
+//            the packed QKV projection the per-head Q/K RMSNorm + NeoX RoPE + KV append
+//            ("per-head Q/K-RMSNorm + NeoX RoPE @ 1e6" in the decoder table; a 128-column
+//            tile is one head).
 // Rows past M are zero-filled by TMA and never stored.  Every wait is bounded; a timeout sets
 // the error word and the CTA finishes without waiting further (TMEM is freed only after the
 // accumulator barrier).
@@ -103,11 +106,49 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The per-head epilogue of the QKV projection on one 128-wide head row v (one thread owns
+// row `row` of the tile; head hd = the tile's column index).
+__device__ __forceinline__ void qkv_rope_row(float (&v)[128], int row, int hd, const QkvRopeEpi& e) {
+    const int p = e.pos0 + row;
+    bf16_t* dst;
+    if (hd >= e.HQ + e.HKV) {   // value head: stored as computed
+        dst = e.vc + ((size_t)(hd - e.HQ - e.HKV) * e.max_seq + p) * 128;
+    } else {
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < 128; ++i) ss = fmaf(v[i], v[i], ss);
+        const float r = rsqrtf(ss / 128.f + e.eps);
+        const bf16_t* g = hd < e.HQ ? e.g_q : e.g_k;
+        const float2* cs = e.rope + (size_t)p * 64;
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+            const uint32_t ga = *reinterpret_cast<const uint32_t*>(g + i);
+            const uint32_t gb = *reinterpret_cast<const uint32_t*>(g + 64 + i);
+            const float4 c2 = *reinterpret_cast<const float4*>(cs + i);   // (cos, sin) of pairs i, i + 1
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const float a = v[i + u] * (r * (u ? bf_hi(ga) : bf_lo(ga)));
+                const float b = v[64 + i + u] * (r * (u ? bf_hi(gb) : bf_lo(gb)));
+                const float c = u ? c2.z : c2.x, sn = u ? c2.w : c2.y;
+                v[i + u] = a * c - b * sn;
+                v[64 + i + u] = b * c + a * sn;
+            }
+        }
+        dst = hd < e.HQ ? e.q + ((size_t)row * e.HQ + hd) * 128
+                        : e.kc + ((size_t)(hd - e.HQ) * e.max_seq + p) * 128;
+    }
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        d4[j] = make_uint4(pack_bf2(v[8 * j], v[8 * j + 1]), pack_bf2(v[8 * j + 2], v[8 * j + 3]),
+                           pack_bf2(v[8 * j + 4], v[8 * j + 5]), pack_bf2(v[8 * j + 6], v[8 * j + 7]));
+}
+
 template <int BN, int MODE, int STAGES>
 __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                                                          const __grid_constant__ CUtensorMap tmB, int M, int K,
                                                          int up_off, float* __restrict__ Cf,
-                                                         bf16_t* __restrict__ Cb, int ldc) {
+                                                         bf16_t* __restrict__ Cb, int ldc, const QkvRopeEpi epi) {
     extern __shared__ __align__(1024) char smem_raw[];
     char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     constexpr int A_BYTES = BM * BK * 2;
@@ -182,7 +223,18 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
         const int q = warp & 3;
         const int row = m0 + 32 * q + lane;
         const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
-        if (GLU) {
+        if constexpr (MODE == GEMM_QKV_ROPE) {
+            static_assert(BN == 128, "one 128-column tile per head");
+            float v[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float t[32];
+                tmem_ld32(taddr + 32 * c, t);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) v[32 * c + k] = t[k];
+            }
+            if (row < M) qkv_rope_row(v, row, blockIdx.x, epi);
+        } else if (GLU) {
 #pragma unroll 1
             for (int c0 = 0; c0 < BN / 2; c0 += 32) {
                 float g[32], u[32];
@@ -272,7 +324,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 
 template <int BN, int MODE, int STAGES>
 cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N, int K, int up_off, float* Cf,
-                      bf16_t* Cb, int ldc, int splits, cudaStream_t s) {
+                      bf16_t* Cb, int ldc, int splits, cudaStream_t s, const QkvRopeEpi& epi = QkvRopeEpi{}) {
     constexpr int smem = STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 256;
     auto kern = gemm_tc_kernel<BN, MODE, STAGES>;
     static bool attr = false;
@@ -283,7 +335,7 @@ cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N
     }
     const int tile_n = (MODE == GEMM_SWIGLU_BF16) ? BN / 2 : BN;
     dim3 grid(N / tile_n, (M + BM - 1) / BM, splits);
-    kern<<<grid, 192, smem, s>>>(ma, mb, M, K, up_off, Cf, Cb, ldc);
+    kern<<<grid, 192, smem, s>>>(ma, mb, M, K, up_off, Cf, Cb, ldc, epi);
     return cudaGetLastError();
 }
 
@@ -319,6 +371,23 @@ cudaError_t launch_gemm_tc(const bf16_t* A, int lda, const bf16_t* W, int M, int
         case GEMM_ATOMIC_F32: return launch_bn<128, GEMM_ATOMIC_F32, 3>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
         default: return cudaErrorInvalidValue;
     }
+}
+
+bool gemm_tc_qkv_rope_supported(const Shape& sh, int lda) {
+    return sh.D == 128 && gemm_tc_supported(sh.qkv_rows(), sh.H, GEMM_STORE_F32, lda);
+}
+
+cudaError_t launch_gemm_tc_qkv_rope(const bf16_t* A, int lda, const bf16_t* W, int M, int K, const QkvRopeEpi& epi,
+                                    cudaStream_t s) {
+    (void)cudaGetLastError();
+    const int N = (epi.HQ + 2 * epi.HKV) * 128;
+    if (M <= 0 || K % BK != 0 || lda % 8 != 0 || !epi.q || !epi.kc || !epi.vc || !epi.rope || epi.pos0 < 0 ||
+        epi.pos0 + M > epi.max_seq)
+        return cudaErrorInvalidValue;
+    CUtensorMap ma, mb;
+    if (!make_map(&ma, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, BM)) return cudaErrorInvalidValue;
+    if (!make_map(&mb, W, (uint64_t)N, (uint64_t)K, (uint64_t)K, 128)) return cudaErrorInvalidValue;
+    return launch_bn<128, GEMM_QKV_ROPE, 6>(ma, mb, M, N, K, 0, nullptr, nullptr, 0, 1, s, epi);
 }
 
 int tc_error_read_and_clear() {

@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import oracle
-from qwen3_prefill_kv_gb300 import synth
+from qwen3_prefill_kv_gb300 import synth, _lib
 from qwen3_prefill_kv_gb300._lib import Decoder, DECODE_PERSISTENT, DECODE_GRAPH
 
 import _harness as H
@@ -56,6 +56,32 @@ def test_teacher_forced_workload(full, name):
     kv_prompt = p.ids.numpy().copy()
     mask = np.ones(kv_prompt.size, bool); mask[wl.audio_offset:wl.audio_offset + wl.n_audio] = False
     assert np.array_equal(hist[:wl.n_prompt][mask], kv_prompt[mask])
+
+
+@pytest.mark.parametrize("name", ["funasr_nano_short", "qwen3_asr_30s"])
+def test_fused_qkv_epilogue_matches_separate_kernels(full, name):
+    """The tcgen05 prefill writes K and V from the QKV GEMM's epilogue (per-head norm + RoPE
+    fused); the CUDA-core prefill runs the GEMM and the norm/RoPE/append kernel separately.
+    Both caches and the prefill logits must agree to bf16 rounding."""
+    w, wd, orc = full
+    wl = synth.WORKLOADS[name]
+    p = synth.make_prompt(wl, seed=0)
+    decs, logits = [], []
+    for impl in (_lib.PREFILL_TCGEN05, _lib.PREFILL_SIMT):
+        d = Decoder(SH, wd, max_seq=wl.n_prompt + 1)
+        d.set_option(_lib.OPT_PREFILL_IMPL, impl)
+        lg = torch.empty(SH.vocab, device="cuda")
+        d.prefill(p.ids, p.audio.cuda(), p.audio_offset, logits=lg)
+        decs.append(d)
+        logits.append(lg.cpu().numpy())
+    for layer in (0, 13, SH.n_layers - 1):
+        for kind in (0, 1):
+            a = decs[0].read_kv(layer, kind, 0, wl.n_prompt).view(np.uint16).astype(np.uint32) << 16
+            b = decs[1].read_kv(layer, kind, 0, wl.n_prompt).view(np.uint16).astype(np.uint32) << 16
+            fa, fb = a.view(np.float32), b.view(np.float32)
+            np.testing.assert_allclose(fa, fb, rtol=0, atol=1e-2 * float(np.abs(fb).max()),
+                                       err_msg=f"layer {layer} kind {kind}")
+    np.testing.assert_allclose(logits[0], logits[1], rtol=0, atol=1e-2 * float(np.abs(logits[1]).max()))
 
 
 def test_persistent_and_graph_decode_agree(full):
