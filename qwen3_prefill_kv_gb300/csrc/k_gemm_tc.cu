@@ -3,7 +3,9 @@
 // map - funasr_nano", LLM decoder table: packed QKV projection, o_proj / down_proj with the
 // residual add, packed gate_up with SwiGLU).
 //
-// One CTA computes one 128 x BN tile with six warps:
+// Persistent: one CTA per resident slot walks work units (128 x BN tile, K-slice) with a
+// stride of the grid size; the accumulator is double-buffered in TMEM so the epilogue of
+// one unit overlaps the MMAs of the next.  Six warps:
 //   warp 0   TMA producer: 2-D tensor-map loads (128-byte swizzle) of the A tile (128 rows x
 //            64 k) and the B tile (BN rows x 64 k; SwiGLU: 64 gate rows + the 64 matching up
 //            rows) into a ring of STAGES shared-memory stages;
@@ -38,6 +40,9 @@ __device__ __forceinline__ void mb_init(uint64_t* b, uint32_t c) {
 __device__ __forceinline__ void mb_expect(uint64_t* b, uint32_t n) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(s32(b)), "r"(n) : "memory");
 }
+__device__ __forceinline__ void mb_arrive(uint64_t* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(s32(b)) : "memory");
+}
 __device__ __forceinline__ bool mb_try(uint64_t* b, uint32_t ph) {
     uint32_t ok;
     asm volatile(
@@ -50,6 +55,17 @@ __device__ __forceinline__ bool mb_try(uint64_t* b, uint32_t ph) {
 __device__ __forceinline__ bool mb_wait(uint64_t* b, uint32_t ph, int code) {
     for (uint32_t i = 0; i < TC_SPIN; ++i)
         if (mb_try(b, ph)) return true;
+    atomicCAS(&g_tc_error, 0, code);
+    return false;
+}
+// As mb_wait, but gives up at once when another role of the CTA has failed (*abort set),
+// and sets *abort itself on a timeout.
+__device__ __forceinline__ bool mb_wait_ab(uint64_t* b, uint32_t ph, int code, volatile int* abort) {
+    for (uint32_t i = 0; i < TC_SPIN; ++i) {
+        if (mb_try(b, ph)) return true;
+        if ((i & 255) == 255 && *abort) return false;
+    }
+    *abort = 1;
     atomicCAS(&g_tc_error, 0, code);
     return false;
 }
@@ -148,148 +164,196 @@ template <int BN, int MODE, int STAGES>
 __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                                                          const __grid_constant__ CUtensorMap tmB, int M, int K,
                                                          int up_off, float* __restrict__ Cf,
-                                                         bf16_t* __restrict__ Cb, int ldc, const QkvRopeEpi epi) {
+                                                         bf16_t* __restrict__ Cb, int ldc, const QkvRopeEpi epi,
+                                                         int tiles_m, int tiles_n, int splits) {
     extern __shared__ __align__(1024) char smem_raw[];
     char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     constexpr int A_BYTES = BM * BK * 2;
     constexpr int B_BYTES = BN * BK * 2;
     constexpr bool GLU = (MODE == GEMM_SWIGLU_BF16);
+    constexpr uint32_t ACC_COLS = 2 * BN;   // double-buffered accumulator
     char* sA = smem;
     char* sB = smem + STAGES * A_BYTES;
     uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
     uint64_t* empty = full + STAGES;
-    uint64_t* accb = empty + STAGES;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(accb + 1);
+    uint64_t* acc_full = empty + STAGES;    // [2]: the MMAs of a unit have completed
+    uint64_t* acc_empty = acc_full + 2;     // [2]: the epilogue has read the buffer (4 warps)
+    uint64_t* fin = acc_empty + 2;          // every MMA issued by this CTA has completed
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(fin + 1);
+    volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.y * BM;
-    const int n0 = blockIdx.x * (GLU ? BN / 2 : BN);   // first output column of the tile
-    // split-K: CTA z of gridDim.z handles k-blocks [kb0, kb0 + nk)
-    const int nkb = K / BK, per = (nkb + gridDim.z - 1) / gridDim.z;
-    const int kb0 = blockIdx.z * per;
-    const int nk = max(0, min(nkb, kb0 + per) - kb0);
+    // work unit u = (split z, tile t): t walks the M tiles fastest, so CTAs running at the
+    // same time share the weight (B) tile through L2; split z covers k-blocks [kb0, kb0 + nk)
+    const int nkb = K / BK, per = (nkb + splits - 1) / splits;
+    const int tiles = tiles_m * tiles_n, units = tiles * splits;
+    auto unit = [&](int u, int& m0, int& nt, int& kb0, int& nk) {
+        const int z = u / tiles, t = u - z * tiles;
+        m0 = (t % tiles_m) * BM;
+        nt = t / tiles_m;
+        kb0 = z * per;
+        nk = max(0, min(nkb, kb0 + per) - kb0);
+    };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
             mb_init(&full[i], 1);
             mb_init(&empty[i], 1);
         }
-        mb_init(accb, 1);
+        for (int i = 0; i < 2; ++i) {
+            mb_init(&acc_full[i], 1);
+            mb_init(&acc_empty[i], 4);
+        }
+        mb_init(fin, 1);
+        *abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 1) tmem_alloc(tslot, BN);
+    if (warp == 1) tmem_alloc(tslot, ACC_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
     if (warp == 0) {
-        if (lane == 0) {   // ---- TMA producer
-            int issued = 0;
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % STAGES, r = kb / STAGES;
-                if (!mb_wait(&empty[s], (r & 1) ^ 1, 1)) break;
-                mb_expect(&full[s], A_BYTES + B_BYTES);
-                tma_2d(sA + s * A_BYTES, &tmA, (kb0 + kb) * BK, m0, &full[s]);
-                if (GLU) {
+        if (lane == 0) {   // ---- TMA producer: one stage ring across all of this CTA's units
+            uint32_t g = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                int m0, nt, kb0, nk;
+                unit(u, m0, nt, kb0, nk);
+                const int n0 = nt * (GLU ? BN / 2 : BN);
+                for (int kb = 0; kb < nk; ++kb, ++g) {
+                    const uint32_t s = g % STAGES, r = g / STAGES;
+                    if (!mb_wait_ab(&empty[s], (r & 1) ^ 1, 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    mb_expect(&full[s], A_BYTES + B_BYTES);
+                    tma_2d(sA + s * A_BYTES, &tmA, (kb0 + kb) * BK, m0, &full[s]);
                     tma_2d(sB + s * B_BYTES, &tmB, (kb0 + kb) * BK, n0, &full[s]);
-                    tma_2d(sB + s * B_BYTES + (BN / 2) * 128, &tmB, (kb0 + kb) * BK, up_off + n0, &full[s]);
-                } else {
-                    tma_2d(sB + s * B_BYTES, &tmB, (kb0 + kb) * BK, n0, &full[s]);
+                    if (GLU) tma_2d(sB + s * B_BYTES + (BN / 2) * 128, &tmB, (kb0 + kb) * BK, up_off + n0, &full[s]);
                 }
-                issued = kb + 1;
             }
-            // copies the MMA warp did not consume (only after an error) must land before exit
-            for (int kb = issued - STAGES > 0 ? issued - STAGES : 0; kb < issued; ++kb)
-                mb_wait(&full[kb % STAGES], (kb / STAGES) & 1, 4);
+            // the last copies issued must land before the CTA exits (after an error they may not
+            // have been consumed)
+            for (uint32_t q = g > (uint32_t)STAGES ? g - STAGES : 0; q < g; ++q)
+                mb_wait(&full[q % STAGES], (q / STAGES) & 1, 4);
         }
     } else if (warp == 1) {
         if (lane == 0) {   // ---- MMA issuer
             constexpr uint32_t idesc = idesc_bf16(BM, BN);
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % STAGES, r = kb / STAGES;
-                if (!mb_wait(&full[s], r & 1, 2)) break;
+            uint32_t g = 0;
+            bool ok = true;
+            int j = 0;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++j) {
+                int m0, nt, kb0, nk;
+                unit(u, m0, nt, kb0, nk);
+                const int buf = j & 1;
+                if (!mb_wait_ab(&acc_empty[buf], ((j >> 1) & 1) ^ 1, 5, abort)) break;
                 tc_fence_after();
-                const uint64_t ad = sw128_desc(sA + s * A_BYTES), bd = sw128_desc(sB + s * B_BYTES);
+                const uint32_t dacc = tmem + (uint32_t)(buf * BN);
+                for (int kb = 0; kb < nk; ++kb, ++g) {
+                    const uint32_t s = g % STAGES, r = g / STAGES;
+                    if (!mb_wait_ab(&full[s], r & 1, 2, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = sw128_desc(sA + s * A_BYTES), bd = sw128_desc(sB + s * B_BYTES);
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk)   // 16 bf16 = 32 B per MMA: +2 in the address field
-                    mma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
-                mma_commit(&empty[s]);
+                    for (int kk = 0; kk < BK / 16; ++kk)   // 16 bf16 = 32 B per MMA: +2 in the address field
+                        mma_bf16(dacc, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+                    mma_commit(&empty[s]);
+                }
+                if (ok) mma_commit(&acc_full[buf]);   // arrives when this unit's MMAs have completed
             }
-            mma_commit(accb);   // arrives once every MMA issued above has completed (nk >= 1: host)
+            mma_commit(fin);   // TMEM is freed only after every issued MMA has completed
+            mb_wait(fin, 0, 6);
         }
     } else {   // ---- epilogue: warps 2..5 cover TMEM lane quarters 2, 3, 0, 1
-        mb_wait(accb, 0, 3);
-        tc_fence_after();
         const int q = warp & 3;
-        const int row = m0 + 32 * q + lane;
-        const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
-        if constexpr (MODE == GEMM_QKV_ROPE) {
-            static_assert(BN == 128, "one 128-column tile per head");
-            float v[128];
+        int j = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
+            int m0, nt, kb0, nk;
+            unit(u, m0, nt, kb0, nk);
+            const int buf = j & 1;
+            if (!mb_wait_ab(&acc_full[buf], (j >> 1) & 1, 3, abort)) break;
+            tc_fence_after();
+            const int row = m0 + 32 * q + lane;
+            const int n0 = nt * (GLU ? BN / 2 : BN);
+            const uint32_t taddr = tmem + (uint32_t)(buf * BN) + ((uint32_t)(32 * q) << 16);
+            if (nk == 0) {
+                // an empty K-slice (never produced by the launcher) contributes nothing
+            } else if constexpr (MODE == GEMM_QKV_ROPE) {
+                static_assert(BN == 128, "one 128-column tile per head");
+                float v[128];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float t[32];
-                tmem_ld32(taddr + 32 * c, t);
+                for (int c = 0; c < 4; ++c) {
+                    float t[32];
+                    tmem_ld32(taddr + 32 * c, t);
 #pragma unroll
-                for (int k = 0; k < 32; ++k) v[32 * c + k] = t[k];
-            }
-            if (row < M) qkv_rope_row(v, row, blockIdx.x, epi);
-        } else if (GLU) {
-#pragma unroll 1
-            for (int c0 = 0; c0 < BN / 2; c0 += 32) {
-                float g[32], u[32];
-                tmem_ld32(taddr + c0, g);
-                tmem_ld32(taddr + BN / 2 + c0, u);
-                if (row < M) {
-                    uint4* dst = reinterpret_cast<uint4*>(Cb + (size_t)row * ldc + n0 + c0);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint4 w;
-                        w.x = pack_bf2(silu(g[8 * j + 0]) * u[8 * j + 0], silu(g[8 * j + 1]) * u[8 * j + 1]);
-                        w.y = pack_bf2(silu(g[8 * j + 2]) * u[8 * j + 2], silu(g[8 * j + 3]) * u[8 * j + 3]);
-                        w.z = pack_bf2(silu(g[8 * j + 4]) * u[8 * j + 4], silu(g[8 * j + 5]) * u[8 * j + 5]);
-                        w.w = pack_bf2(silu(g[8 * j + 6]) * u[8 * j + 6], silu(g[8 * j + 7]) * u[8 * j + 7]);
-                        dst[j] = w;
-                    }
+                    for (int k = 0; k < 32; ++k) v[32 * c + k] = t[k];
                 }
-            }
-        } else {
+                if (row < M) qkv_rope_row(v, row, nt, epi);
+            } else if constexpr (GLU) {
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                float v[32];
-                tmem_ld32(taddr + c0, v);
-                if (row < M) {
-                    if (MODE == GEMM_STORE_BF16) {
+                for (int c0 = 0; c0 < BN / 2; c0 += 32) {
+                    float gv[32], uv[32];
+                    tmem_ld32(taddr + c0, gv);
+                    tmem_ld32(taddr + BN / 2 + c0, uv);
+                    if (row < M) {
                         uint4* dst = reinterpret_cast<uint4*>(Cb + (size_t)row * ldc + n0 + c0);
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            dst[j] = make_uint4(pack_bf2(v[8 * j], v[8 * j + 1]), pack_bf2(v[8 * j + 2], v[8 * j + 3]),
-                                                pack_bf2(v[8 * j + 4], v[8 * j + 5]), pack_bf2(v[8 * j + 6], v[8 * j + 7]));
-                    } else {
-                        float4* dst = reinterpret_cast<float4*>(Cf + (size_t)row * ldc + n0 + c0);
+                        for (int jj = 0; jj < 4; ++jj) {
+                            uint4 w;
+                            w.x = pack_bf2(silu(gv[8 * jj + 0]) * uv[8 * jj + 0], silu(gv[8 * jj + 1]) * uv[8 * jj + 1]);
+                            w.y = pack_bf2(silu(gv[8 * jj + 2]) * uv[8 * jj + 2], silu(gv[8 * jj + 3]) * uv[8 * jj + 3]);
+                            w.z = pack_bf2(silu(gv[8 * jj + 4]) * uv[8 * jj + 4], silu(gv[8 * jj + 5]) * uv[8 * jj + 5]);
+                            w.w = pack_bf2(silu(gv[8 * jj + 6]) * uv[8 * jj + 6], silu(gv[8 * jj + 7]) * uv[8 * jj + 7]);
+                            dst[jj] = w;
+                        }
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(taddr + c0, v);
+                    if (row < M) {
+                        if (MODE == GEMM_STORE_BF16) {
+                            uint4* dst = reinterpret_cast<uint4*>(Cb + (size_t)row * ldc + n0 + c0);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            float4 o = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                            if (MODE == GEMM_ATOMIC_F32) {   // split-K partials: vector fp32 reductions
-                                atomicAdd(dst + j, o);
-                                continue;
+                            for (int jj = 0; jj < 4; ++jj)
+                                dst[jj] = make_uint4(pack_bf2(v[8 * jj], v[8 * jj + 1]), pack_bf2(v[8 * jj + 2], v[8 * jj + 3]),
+                                                     pack_bf2(v[8 * jj + 4], v[8 * jj + 5]), pack_bf2(v[8 * jj + 6], v[8 * jj + 7]));
+                        } else {
+                            float4* dst = reinterpret_cast<float4*>(Cf + (size_t)row * ldc + n0 + c0);
+#pragma unroll
+                            for (int jj = 0; jj < 8; ++jj) {
+                                float4 o = make_float4(v[4 * jj], v[4 * jj + 1], v[4 * jj + 2], v[4 * jj + 3]);
+                                if (MODE == GEMM_ATOMIC_F32) {   // split-K partials: vector fp32 reductions
+                                    atomicAdd(dst + jj, o);
+                                    continue;
+                                }
+                                if (MODE == GEMM_ADD_F32) {
+                                    const float4 c = dst[jj];
+                                    o.x += c.x; o.y += c.y; o.z += c.z; o.w += c.w;
+                                }
+                                dst[jj] = o;
                             }
-                            if (MODE == GEMM_ADD_F32) {
-                                const float4 c = dst[j];
-                                o.x += c.x; o.y += c.y; o.z += c.z; o.w += c.w;
-                            }
-                            dst[j] = o;
                         }
                     }
                 }
             }
+            tc_fence_before();   // this warp's accumulator reads are complete
+            __syncwarp();
+            if (lane == 0) mb_arrive(&acc_empty[buf]);
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, BN);
+        tmem_dealloc(tmem, ACC_COLS);
     }
 }
 
@@ -327,15 +391,22 @@ cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N
                       bf16_t* Cb, int ldc, int splits, cudaStream_t s, const QkvRopeEpi& epi = QkvRopeEpi{}) {
     constexpr int smem = STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 256;
     auto kern = gemm_tc_kernel<BN, MODE, STAGES>;
-    static bool attr = false;
-    if (!attr) {
+    static int resident = 0;   // CTAs of this instantiation that fit on the device at once
+    if (!resident) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        int dev = 0, sms = 0, per_sm = 0;
+        if (e == cudaSuccess) e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 192, smem);
         if (e != cudaSuccess) return e;
-        attr = true;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+        resident = sms * per_sm;
     }
     const int tile_n = (MODE == GEMM_SWIGLU_BF16) ? BN / 2 : BN;
-    dim3 grid(N / tile_n, (M + BM - 1) / BM, splits);
-    kern<<<grid, 192, smem, s>>>(ma, mb, M, K, up_off, Cf, Cb, ldc, epi);
+    const int tiles_m = (M + BM - 1) / BM, tiles_n = N / tile_n;
+    const long long units = (long long)tiles_m * tiles_n * splits;
+    const int grid = (int)(units < resident ? units : resident);   // persistent: each CTA walks units
+    kern<<<grid, 192, smem, s>>>(ma, mb, M, K, up_off, Cf, Cb, ldc, epi, tiles_m, tiles_n, splits);
     return cudaGetLastError();
 }
 
