@@ -6,6 +6,9 @@
 // GQA 16/8).  The softmax is evaluated online over key tiles (running max and sum), i.e. the
 // max-subtracted softmax rearranged tile by tile.
 //
+// Two kernels.  When each kv head serves an even number of q heads (GQA 16/8), the paired-head
+// kernel below (attn_prefill_tc2_kernel) runs; otherwise this one.
+//
 // One CTA = one 128-query tile of one q head; six warps:
 //   warp 0    TMA: the Q tile once, then K and V tiles of 128 keys into a 2-stage ring
 //             (3-D tensor maps over [T][HQ][D] and [HKV][max_seq][D], 128-byte swizzle);
@@ -344,6 +347,334 @@ __global__ void __launch_bounds__(192, 1) attn_prefill_tc_kernel(const __grid_co
     }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Paired-head variant: one CTA = one 128-query tile of the two q heads 2c and 2c + 1, which
+// share kv head g (HQ / HKV even), so every K and V tile is fetched once for two heads and the
+// two heads' softmax warpgroups overlap each other's tensor-core work.  Ten warps:
+//   warp 0    TMA: both Q tiles once, then K_0, K_1, V_0, K_2, V_1, ... (the order the MMAs
+//             consume them) into a 3-slot ring of 32 KB tiles;
+//   warp 1    allocates 512 TMEM columns (per head: S at 256h, O at 256h + 128) and issues
+//             S_j(h) = Q_h K_j^T as soon as head h has read S_{j-1}(h) out of TMEM, and
+//             O(h) += P_j(h) V_j once P_j(h) is in shared memory (O accumulates in TMEM);
+//   warps 2-5 / 6-9  softmax of head 0 / head 1, one query row per thread: S_j read from TMEM
+//             once (128 fp32 values in registers), masked row max, P_j = exp2(s*c - m) as
+//             bf16 into swizzled shared memory.  The running max m is raised only when a tile
+//             exceeds it by more than 2^8 (P stays <= 256); only then is the row's O in TMEM
+//             rescaled, after the previous P.V has completed.  Final O / l stored bf16.
+// The result equals the max-subtracted softmax: every P_j and the running sum l use the same
+// m as the part of O they are added to.
+constexpr int NSLOT = 3;
+constexpr float LAZY_RESCALE_LOG2 = 8.f;
+
+struct Fa2Bars {
+    uint64_t q_full, ring_full[NSLOT], ring_empty[NSLOT], s_full[2], s_free[2], p_full[2], p_free[2], fin;
+    uint32_t tmem;
+    int abort;
+};
+
+__device__ __forceinline__ bool mb_wait_ab(uint64_t* b, uint32_t ph, int code, volatile int* abort) {
+    for (uint32_t i = 0; i < FA_SPIN; ++i) {
+        if (mb_try(b, ph)) return true;
+        if ((i & 255) == 255 && *abort) return false;
+    }
+    *abort = 1;
+    atomicCAS(&g_fa_error, 0, code);
+    return false;
+}
+// Four 32-column TMEM loads of this warp's lanes issued back to back, then one wait; the
+// wait names every destination register so no use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[4][32]) {
+    tmem_ld32_issue(taddr, r[0]);
+    tmem_ld32_issue(taddr + 32, r[1]);
+    tmem_ld32_issue(taddr + 64, r[2]);
+    tmem_ld32_issue(taddr + 96, r[3]);
+    tmem_wait_ld(r[0]);
+    tmem_wait_ld(r[1]);
+    tmem_wait_ld(r[2]);
+    tmem_wait_ld(r[3]);
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+                 :
+                 : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(320, 1) attn_prefill_tc2_kernel(const __grid_constant__ CUtensorMap tmQ,
+                                                                  const __grid_constant__ CUtensorMap tmK,
+                                                                  const __grid_constant__ CUtensorMap tmV, int T,
+                                                                  int HQ, int HKV, int pos0, bf16_t* __restrict__ O,
+                                                                  float scale_log2) {
+    extern __shared__ __align__(1024) char smem_raw[];
+    char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    char* sQ = smem;                                  // 2 heads x 32 KB
+    char* sRing = sQ + 2 * TILE_BYTES;                // NSLOT x 32 KB (K or V tiles)
+    char* sP = sRing + NSLOT * TILE_BYTES;            // 2 heads x 32 KB
+    Fa2Bars* B = reinterpret_cast<Fa2Bars*>(sP + 2 * TILE_BYTES);
+    volatile int* abort = &B->abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ntq = (T + QT - 1) / QT;
+    const int qtile = ntq - 1 - (int)blockIdx.y;     // longest causal rows first (y is dispatched last)
+    const int h0 = 2 * (int)blockIdx.x, g = h0 / (HQ / HKV);
+    const int q0 = qtile * QT;
+    const int L = pos0 + T;
+    const int kend = min(L, pos0 + q0 + QT);          // keys [0, kend) can be visible to this tile
+    const int nt = (kend + KT - 1) / KT;
+
+    if (threadIdx.x == 0) {
+        mb_init(&B->q_full, 1);
+        for (int i = 0; i < NSLOT; ++i) {
+            mb_init(&B->ring_full[i], 1);
+            mb_init(&B->ring_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mb_init(&B->s_full[i], 1);
+            mb_init(&B->s_free[i], 4);
+            mb_init(&B->p_full[i], 4);
+            mb_init(&B->p_free[i], 1);
+        }
+        mb_init(&B->fin, 1);
+        B->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(s32(&B->tmem))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = B->tmem;
+
+    if (warp == 0) {
+        if (lane == 0) {   // ---- TMA producer: items in consumption order K0, K1, V0, K2, V1, ...
+            mb_expect(&B->q_full, 2 * TILE_BYTES);
+            for (int hh = 0; hh < 2; ++hh) {
+                tma_3d(sQ + hh * TILE_BYTES, &tmQ, 0, h0 + hh, q0, &B->q_full);
+                tma_3d(sQ + hh * TILE_BYTES + BLK, &tmQ, 64, h0 + hh, q0, &B->q_full);
+            }
+            uint32_t n = 0;
+            bool ok = true;
+            auto put = [&](const CUtensorMap* map, int j) {
+                const uint32_t slot = n % NSLOT, r = n / NSLOT;
+                if (!mb_wait_ab(&B->ring_empty[slot], (r & 1) ^ 1, 31, abort)) return false;
+                char* dst = sRing + slot * TILE_BYTES;
+                mb_expect(&B->ring_full[slot], TILE_BYTES);
+                tma_3d(dst, map, 0, j * KT, g, &B->ring_full[slot]);
+                tma_3d(dst + BLK, map, 64, j * KT, g, &B->ring_full[slot]);
+                ++n;
+                return true;
+            };
+            for (int j = 0; j < nt && ok; ++j) {
+                ok = put(&tmK, j);
+                if (ok && j >= 1) ok = put(&tmV, j - 1);
+            }
+            if (ok) put(&tmV, nt - 1);
+            // every copy issued must land before the CTA exits
+            mb_wait(&B->q_full, 0, 32);
+            for (uint32_t i = n > (uint32_t)NSLOT ? n - NSLOT : 0; i < n; ++i)
+                mb_wait(&B->ring_full[i % NSLOT], (i / NSLOT) & 1, 33);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {   // ---- MMA issuer
+            constexpr uint32_t id_s = idesc_fa(false), id_o = idesc_fa(true);
+            uint32_t n = 0;
+            bool ok = mb_wait_ab(&B->q_full, 0, 34, abort);
+            auto pv = [&](int i) {   // O(h) += P_i(h) V_i for both heads
+                const uint32_t slot = n % NSLOT;
+                if (!mb_wait_ab(&B->ring_full[slot], (n / NSLOT) & 1, 35, abort)) return false;
+                const char* v = sRing + slot * TILE_BYTES;
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (!mb_wait_ab(&B->p_full[hh], i & 1, 36, abort)) return false;
+                    tc_fence_after();
+                    const char* pp = sP + hh * TILE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t ad = desc_kmajor(pp + (kk >> 2) * BLK) + 2 * (kk & 3);
+                        const uint64_t bd = desc_mnmajor(v) + (uint64_t)((kk * 16 * 128) >> 4);
+                        mma_bf16(tmem + 256 * hh + 128, ad, bd, id_o, (i > 0 || kk != 0) ? 1u : 0u);
+                    }
+                    mma_commit(&B->p_free[hh]);
+                }
+                mma_commit(&B->ring_empty[slot]);
+                ++n;
+                return true;
+            };
+            for (int j = 0; j < nt && ok; ++j) {
+                const uint32_t slot = n % NSLOT;
+                ok = mb_wait_ab(&B->ring_full[slot], (n / NSLOT) & 1, 37, abort);
+                if (!ok) break;
+                const char* k = sRing + slot * TILE_BYTES;
+                for (int hh = 0; hh < 2 && ok; ++hh) {
+                    if (j >= 1) ok = mb_wait_ab(&B->s_free[hh], (j - 1) & 1, 38, abort);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const char* qq = sQ + hh * TILE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t ad = desc_kmajor(qq + (kk >> 2) * BLK) + 2 * (kk & 3);
+                        const uint64_t bd = desc_kmajor(k + (kk >> 2) * BLK) + 2 * (kk & 3);
+                        mma_bf16(tmem + 256 * hh, ad, bd, id_s, kk != 0);
+                    }
+                    mma_commit(&B->s_full[hh]);
+                }
+                if (!ok) break;
+                mma_commit(&B->ring_empty[slot]);
+                ++n;
+                if (j >= 1) ok = pv(j - 1);
+            }
+            if (ok && nt >= 1) pv(nt - 1);
+            mma_commit(&B->fin);   // TMEM is freed only after every issued MMA has completed
+            mb_wait(&B->fin, 0, 39);
+        }
+    } else {   // ---- softmax: warps 2-5 head 0, warps 6-9 head 1; TMEM lane quarter = warp % 4
+        const int hh = (warp - 2) >> 2;
+        const int q = warp & 3;
+        const int row = 32 * q + lane;
+        const int qpos = pos0 + q0 + row;
+        const uint32_t sadr = tmem + ((uint32_t)(32 * q) << 16) + 256 * hh;
+        const uint32_t oadr = sadr + 128;
+        char* pst = sP + hh * TILE_BYTES;
+        float m_run = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nt && ok; ++j) {
+            // a tile wholly below the diagonal (every key visible to every row) needs no mask
+            const bool full = (j * KT + KT - 1 <= pos0 + q0) && (j * KT + KT <= L);
+            // warp-uniform outcome: the TMEM loads below are warp-collective
+            if (!__all_sync(0xffffffffu, mb_wait_ab(&B->s_full[hh], j & 1, 40, abort))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sr[4][32];
+            tmem_ld128(sadr, sr);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mb_arrive(&B->s_free[hh]);   // S may be overwritten by S_{j+1}
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (full) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) mx4[k & 3] = fmaxf(mx4[k & 3], __uint_as_float(sr[c][k]));
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) {
+                        const int key = j * KT + 32 * c + k;
+                        if (key <= qpos && key < L) mx4[k & 3] = fmaxf(mx4[k & 3], __uint_as_float(sr[c][k]));
+                    }
+            }
+            const float m_tile = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * scale_log2;
+            const bool need = m_tile > m_run + LAZY_RESCALE_LOG2;   // false while both are -inf
+            const bool any = __any_sync(0xffffffffu, need) && j > 0;
+            float corr = 1.f;
+            if (need) {
+                corr = (m_run == -INFINITY) ? 0.f : ex2(m_run - m_tile);
+                m_run = m_tile;
+            }
+            // P_j = exp2(s * c - m) (0 where masked), packed to bf16 pairs in place
+            float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+            const bool live = m_run != -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int k = 0; k < 32; k += 2) {
+                    float p0, p1;
+                    if (full) {
+                        p0 = ex2(fmaf(__uint_as_float(sr[c][k]), scale_log2, -m_run));
+                        p1 = ex2(fmaf(__uint_as_float(sr[c][k + 1]), scale_log2, -m_run));
+                    } else {
+                        const int key = j * KT + 32 * c + k;
+                        p0 = (live && key <= qpos && key < L) ? ex2(fmaf(__uint_as_float(sr[c][k]), scale_log2, -m_run)) : 0.f;
+                        p1 = (live && key + 1 <= qpos && key + 1 < L)
+                                 ? ex2(fmaf(__uint_as_float(sr[c][k + 1]), scale_log2, -m_run))
+                                 : 0.f;
+                    }
+                    ls4[k & 3] += p0;
+                    ls4[(k + 1) & 3] += p1;
+                    sr[c][k >> 1] = pack_bf2(p0, p1);   // k >> 1 < k for k >= 2: never overwrites an unread value
+                }
+            l = l * corr + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
+            if (j >= 1) {   // P(h) and O(h) are free once P_{j-1}(h) V_{j-1} has completed
+                if (!__all_sync(0xffffffffu, mb_wait_ab(&B->p_free[hh], (j - 1) & 1, 41, abort))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (any) {
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32_issue(oadr + 32 * c, o);
+                        tmem_wait_ld(o);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * corr);
+                        tmem_st32(oadr + 32 * c, o);
+                    }
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                }
+            }
+            // P_j into the swizzled K-major layout the MMA reads (rows 128 B, 16-byte chunk c
+            // of row r at chunk position c ^ (r & 7)); chunk u of column block c holds keys
+            // 32c + 8u .. 32c + 8u + 7, i.e. packed words sr[c][4u .. 4u + 3]
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int key0 = 32 * c + 8 * u;
+                    const int blk = key0 >> 6, ch = (key0 & 63) >> 3;
+                    *reinterpret_cast<uint4*>(pst + blk * BLK + row * 128 + ((ch ^ (row & 7)) << 4)) =
+                        make_uint4(sr[c][4 * u], sr[c][4 * u + 1], sr[c][4 * u + 2], sr[c][4 * u + 3]);
+                }
+            tc_fence_before();
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // P is read by the tensor cores
+            __syncwarp();
+            if (lane == 0) mb_arrive(&B->p_full[hh]);
+        }
+        if (ok && nt >= 1 && __all_sync(0xffffffffu, mb_wait_ab(&B->p_free[hh], (nt - 1) & 1, 42, abort))) {
+            tc_fence_after();
+            uint32_t orr[4][32];
+            tmem_ld128(oadr, orr);
+            const int t = q0 + row;
+            if (t < T) {
+                const float inv = 1.f / l;
+                uint4* dst = reinterpret_cast<uint4*>(O + (size_t)t * HQ * HD + (size_t)(h0 + hh) * HD);
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint32_t* w = &orr[c][8 * u];
+                        dst[4 * c + u] = make_uint4(pack_bf2(__uint_as_float(w[0]) * inv, __uint_as_float(w[1]) * inv),
+                                                    pack_bf2(__uint_as_float(w[2]) * inv, __uint_as_float(w[3]) * inv),
+                                                    pack_bf2(__uint_as_float(w[4]) * inv, __uint_as_float(w[5]) * inv),
+                                                    pack_bf2(__uint_as_float(w[6]) * inv, __uint_as_float(w[7]) * inv));
+                    }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+    }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn3() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
@@ -402,15 +733,28 @@ cudaError_t launch_attention_prefill_tc(const bf16_t* Q, int T, const Shape& sh,
     if (!make_map3(&mv, v_cache, D, (uint64_t)sh.max_seq, (uint64_t)sh.HKV, D * 2, (uint64_t)sh.max_seq * D * 2, KT, 1))
         return cudaErrorInvalidValue;
     constexpr int smem = 7 * TILE_BYTES + 1024 + 256;
+    static_assert(sizeof(FaBars) <= 256 && sizeof(Fa2Bars) <= 256, "barrier block");
+    const float scale_log2 = 1.4426950408889634f / sqrtf(128.f);
+    const int ntq = (T + QT - 1) / QT;
+    if ((sh.HQ / sh.HKV) % 2 == 0) {   // two q heads of one kv group per CTA
+        static bool attr2 = false;
+        if (!attr2) {
+            cudaError_t e = cudaFuncSetAttribute(attn_prefill_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+            attr2 = true;
+        }
+        // x = head pair, y = query tile rank: CTAs are dispatched longest causal rows first
+        attn_prefill_tc2_kernel<<<dim3(sh.HQ / 2, ntq), 320, smem, s>>>(mq, mk, mv, T, sh.HQ, sh.HKV, pos0, O,
+                                                                         scale_log2);
+        return cudaGetLastError();
+    }
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(attn_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    dim3 grid((T + QT - 1) / QT, sh.HQ);
-    const float scale_log2 = 1.4426950408889634f / sqrtf(128.f);
-    attn_prefill_tc_kernel<<<grid, 192, smem, s>>>(mq, mk, mv, T, sh.HQ, sh.HKV, pos0, O, scale_log2);
+    attn_prefill_tc_kernel<<<dim3(ntq, sh.HQ), 192, smem, s>>>(mq, mk, mv, T, sh.HQ, sh.HKV, pos0, O, scale_log2);
     return cudaGetLastError();
 }
 

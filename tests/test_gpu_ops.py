@@ -67,7 +67,8 @@ def test_gemm_splitk_atomic(M, N, K, splits):
 
 
 ATTN_CASES = [(77, 4, 2, 32, 0), (64, 16, 8, 128, 0), (200, 16, 8, 128, 0), (33, 4, 2, 32, 40), (5, 16, 8, 128, 100),
-              (415, 16, 8, 128, 0), (1000, 16, 8, 128, 0), (130, 4, 4, 128, 0), (300, 8, 1, 128, 0)]
+              (415, 16, 8, 128, 0), (1000, 16, 8, 128, 0), (130, 4, 4, 128, 0), (300, 8, 1, 128, 0),
+              (300, 16, 8, 128, 77), (2100, 16, 8, 128, 0)]
 
 
 @pytest.mark.parametrize("impl", [_lib.IMPL_SIMT, _lib.IMPL_TCGEN05], ids=["simt", "tcgen05"])
@@ -87,6 +88,28 @@ def test_attention_prefill(impl, T, HQ, HKV, D, pos0):
     ref = oracle.causal_gqa_attention(Q.double().numpy(), K[:, :L].permute(1, 0, 2).double().numpy(),
                                       Vv[:, :L].permute(1, 0, 2).double().numpy(),
                                       np.arange(pos0, pos0 + T), np.arange(L)).reshape(T, HQ * D)
+    got = O.cpu().double().numpy()
+    assert np.abs(got - ref).max() <= 1e-2 * np.abs(ref).max()
+
+
+@pytest.mark.parametrize("HQ,HKV", [(16, 8), (4, 4)])
+def test_attention_prefill_rising_scores(HQ, HKV):
+    """Keys whose scale grows with position make each key tile's row maximum exceed the
+    running one by more than 2^8 (in the exp2 domain) every few tiles, so the tensor-core
+    kernel's deferred rescaling of O is exercised; the softmax must still be exact."""
+    T, D, pos0 = 1000, 128, 0
+    L, max_seq = T, T
+    g = torch.Generator().manual_seed(11)
+    Q = (0.5 + 0.1 * torch.randn(T, HQ, D, generator=g)).to(torch.bfloat16)
+    c = (torch.arange(max_seq, dtype=torch.float32) / 100.0).view(1, max_seq, 1)
+    K = (c * (0.5 + 0.1 * torch.randn(HKV, max_seq, D, generator=g))).to(torch.bfloat16)
+    Vv = _bf16((HKV, max_seq, D), 12)
+    O = torch.zeros(T, HQ * D, dtype=torch.bfloat16, device="cuda")
+    _lib.attention_prefill(Q.cuda(), T, HQ, HKV, D, max_seq, pos0, K.cuda(), Vv.cuda(), O, impl=_lib.IMPL_TCGEN05)
+    torch.cuda.synchronize()
+    _lib.device_error()
+    ref = oracle.causal_gqa_attention(Q.double().numpy(), K.permute(1, 0, 2).double().numpy(),
+                                      Vv.permute(1, 0, 2).double().numpy(), np.arange(T), np.arange(L)).reshape(T, HQ * D)
     got = O.cpu().double().numpy()
     assert np.abs(got - ref).max() <= 1e-2 * np.abs(ref).max()
 
