@@ -40,6 +40,14 @@ int qdec_op_gemm(const void *A, int32_t lda, const void *W, int32_t M, int32_t N
 int qdec_op_gemm_splitk(const void *A, int32_t lda, const void *W, int32_t M, int32_t N, int32_t K, int32_t splits,
                         float *C, int32_t ldc, void *stream);
 
+/* Tile width of the tcgen05 GEMMs (qdec_op_gemm and the context's prefill):
+ * 0 lets the library choose per shape (128 x 256 tiles when the problem has
+ * enough tiles to fill the SMs, else 128 x 128), 128 or 256 forces one (a
+ * shape that a 256-wide tile does not divide still uses 128).  Process-wide
+ * and not thread-safe: meant for tuning and tests.  Returns the previous
+ * setting, or QDEC_E_INVALID_ARG for any other value. */
+int qdec_op_gemm_tile_width(int32_t bn);
+
 /* Synchronises the device and reports whether a tensor-core kernel launched
  * through these entry points gave up on a bounded wait since the last call:
  * QDEC_OK, or QDEC_E_TIMEOUT (the flag is then cleared). */

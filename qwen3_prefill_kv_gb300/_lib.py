@@ -72,6 +72,7 @@ SIGNATURES = [
     ("qdec_kernel_launches", C.c_uint64, []),
     ("qdec_op_gemm", C.c_int, [_VP, _I32, _VP, _I32, _I32, _I32, _I32, _I32, _VP, _I32, _I32, _VP]),
     ("qdec_op_device_error", C.c_int, []),
+    ("qdec_op_gemm_tile_width", C.c_int, [C.c_int32]),
     ("qdec_op_gemm_splitk", C.c_int, [_VP, _I32, _VP, _I32, _I32, _I32, _I32, _VP, _I32, _VP]),
     ("qdec_op_attention_prefill", C.c_int, [_VP, _I32, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _I32, _VP]),
     ("qdec_op_lm_head_scratch_bytes", _SZ, [_I32]),
@@ -257,6 +258,13 @@ def gemm_splitk(A, W, M, N, K, splits, C_out, lda=None, ldc=None, stream=None) -
     lib = load()
     _check(lib.qdec_op_gemm_splitk(_ptr(A), lda if lda is not None else K, _ptr(W), M, N, K, splits, _ptr(C_out),
                                    ldc if ldc is not None else N, _stream_handle(stream)))
+
+
+def gemm_tile_width(bn: int) -> int:
+    """Forces the tcgen05 GEMM tile width (128 or 256; 0 = per shape); returns the previous one."""
+    rc = int(load().qdec_op_gemm_tile_width(int(bn)))
+    _check(min(rc, 0))
+    return rc
 
 
 def device_error() -> None:

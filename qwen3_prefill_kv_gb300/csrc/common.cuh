@@ -76,6 +76,9 @@ cudaError_t launch_gemm_simt(const bf16_t* A, int lda, const bf16_t* W, int M, i
 // lda % 8 == 0, N % 128 == 0 (SwiGLU: N % 64 == 0) and 16-byte aligned A, W.
 bool gemm_tc_supported(int N, int K, int mode, int lda);
 // GEMM_ATOMIC_F32 (C += acc with fp32 vector atomics) may split K over `splits` CTAs per tile.
+// Forces the tcgen05 GEMM's tile width (128 or 256; 0 = chosen per shape); returns the previous
+// setting.  Process-wide, not thread-safe: for tuning and tests.
+int set_gemm_tile_width(int bn);
 cudaError_t launch_gemm_tc(const bf16_t* A, int lda, const bf16_t* W, int M, int N, int K, int mode, int up_off,
                            float* Cf, bf16_t* Cb, int ldc, cudaStream_t s, int splits = 1);
 // The packed QKV projection with the per-head epilogue fused (head_dim 128, one head per

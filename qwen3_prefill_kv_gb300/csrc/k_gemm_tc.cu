@@ -3,19 +3,19 @@
 // map - funasr_nano", LLM decoder table: packed QKV projection, o_proj / down_proj with the
 // residual add, packed gate_up with SwiGLU).
 //
-// Persistent: one CTA per resident slot walks work units (128 x BN tile, K-slice) with a
+// Persistent: one CTA per resident slot walks work units (128 x BN tile, BN = 128 or 256, K-slice) with a
 // stride of the grid size; the accumulator is double-buffered in TMEM so the epilogue of
 // one unit overlaps the MMAs of the next.  Six warps:
 //   warp 0   TMA producer: 2-D tensor-map loads (128-byte swizzle) of the A tile (128 rows x
-//            64 k) and the B tile (BN rows x 64 k; SwiGLU: 64 gate rows + the 64 matching up
-//            rows) into a ring of STAGES shared-memory stages;
-//   warp 1   allocates BN TMEM columns and issues tcgen05.mma (M = 128, N = BN, K = 16) from
+//            64 k) and the B tile (BN rows x 64 k; SwiGLU: BN/2 gate rows + the BN/2 matching
+//            up rows) into a ring of STAGES shared-memory stages;
+//   warp 1   allocates 2 BN TMEM columns and issues tcgen05.mma (M = 128, N = BN, K = 16) from
 //            one thread, committing each stage back to its empty barrier;
 //   warps 2-5 epilogue: tcgen05.ld of the accumulator (one TMEM lane = one output row),
 //            then store / residual add / SwiGLU / split-K atomics to global memory, or for
 //            the packed QKV projection the per-head Q/K RMSNorm + NeoX RoPE + KV append
-//            ("per-head Q/K-RMSNorm + NeoX RoPE @ 1e6" in the decoder table; a 128-column
-//            tile is one head).
+//            ("per-head Q/K-RMSNorm + NeoX RoPE @ 1e6" in the decoder table; every 128
+//            columns of a tile are one head).
 // Rows past M are zero-filled by TMA and never stored.  Every wait is bounded; a timeout sets
 // the error word and the CTA finishes without waiting further (TMEM is freed only after the
 // accumulator barrier).
@@ -160,6 +160,10 @@ __device__ __forceinline__ void qkv_rope_row(float (&v)[128], int row, int hd, c
                            pack_bf2(v[8 * j + 4], v[8 * j + 5]), pack_bf2(v[8 * j + 6], v[8 * j + 7]));
 }
 
+// Rows of one TMA box of the B (weight) tile: a SwiGLU tile is BN/2 gate rows + BN/2 up rows;
+// otherwise boxes of 128 rows.
+__host__ __device__ constexpr int b_box_rows(int BN, int MODE) { return MODE == GEMM_SWIGLU_BF16 ? BN / 2 : 128; }
+
 template <int BN, int MODE, int STAGES>
 __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                                                          const __grid_constant__ CUtensorMap tmB, int M, int K,
@@ -171,7 +175,9 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
     constexpr int A_BYTES = BM * BK * 2;
     constexpr int B_BYTES = BN * BK * 2;
     constexpr bool GLU = (MODE == GEMM_SWIGLU_BF16);
-    constexpr uint32_t ACC_COLS = 2 * BN;   // double-buffered accumulator
+    constexpr int B_BOX = b_box_rows(BN, MODE), B_LOADS = BN / B_BOX;
+    static_assert(BN == 128 || BN == 256, "tile width");
+    constexpr uint32_t ACC_COLS = 2 * BN;   // double-buffered accumulator (512 columns at most)
     char* sA = smem;
     char* sB = smem + STAGES * A_BYTES;
     uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
@@ -229,8 +235,12 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
                     }
                     mb_expect(&full[s], A_BYTES + B_BYTES);
                     tma_2d(sA + s * A_BYTES, &tmA, (kb0 + kb) * BK, m0, &full[s]);
-                    tma_2d(sB + s * B_BYTES, &tmB, (kb0 + kb) * BK, n0, &full[s]);
-                    if (GLU) tma_2d(sB + s * B_BYTES + (BN / 2) * 128, &tmB, (kb0 + kb) * BK, up_off + n0, &full[s]);
+                    // B: BN rows in boxes of B_BOX rows stacked in shared memory (SwiGLU: the
+                    // gate rows, then the matching up rows)
+#pragma unroll
+                    for (int b = 0; b < B_LOADS; ++b)
+                        tma_2d(sB + s * B_BYTES + b * B_BOX * 128, &tmB, (kb0 + kb) * BK,
+                               GLU ? (b ? up_off + n0 : n0) : n0 + b * B_BOX, &full[s]);
                 }
             }
             // the last copies issued must land before the CTA exits (after an error they may not
@@ -283,17 +293,19 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
             const uint32_t taddr = tmem + (uint32_t)(buf * BN) + ((uint32_t)(32 * q) << 16);
             if (nk == 0) {
                 // an empty K-slice (never produced by the launcher) contributes nothing
-            } else if constexpr (MODE == GEMM_QKV_ROPE) {
-                static_assert(BN == 128, "one 128-column tile per head");
-                float v[128];
+            } else if constexpr (MODE == GEMM_QKV_ROPE) {   // one head per 128 columns
+#pragma unroll 1
+                for (int hb = 0; hb < BN / 128; ++hb) {
+                    float v[128];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float t[32];
-                    tmem_ld32(taddr + 32 * c, t);
+                    for (int c = 0; c < 4; ++c) {
+                        float t[32];
+                        tmem_ld32(taddr + 128 * hb + 32 * c, t);
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) v[32 * c + k] = t[k];
+                        for (int k = 0; k < 32; ++k) v[32 * c + k] = t[k];
+                    }
+                    if (row < M) qkv_rope_row(v, row, nt * (BN / 128) + hb, epi);
                 }
-                if (row < M) qkv_rope_row(v, row, nt, epi);
             } else if constexpr (GLU) {
 #pragma unroll 1
                 for (int c0 = 0; c0 < BN / 2; c0 += 32) {
@@ -410,7 +422,42 @@ cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N
     return cudaGetLastError();
 }
 
+// Tile width.  A 128 x 256 tile moves 1.33x fewer operand bytes per FLOP than a 128 x 128 one,
+// but has half as many tiles to spread over the SMs (one CTA per SM either way); the wider
+// tile is taken when its rounds of tiles, weighted by WIDE_COST (time of a 256-wide tile
+// relative to two 128-wide ones), cost less.  set_gemm_tile_width() forces a width.
+constexpr double WIDE_COST = 0.75;
+int g_tile_width = 0;   // 0 = chosen per shape; 128 or 256 = forced
+int gemm_bn_override() { return g_tile_width; }
+int device_sms() {
+    static int sms = 0;
+    if (!sms) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            sms = 148;
+        }
+    }
+    return sms;
+}
+bool use_wide_tiles(int M, int N, int mode) {
+    const bool glu = mode == GEMM_SWIGLU_BF16;
+    const int tn128 = glu ? 64 : 128, tn256 = glu ? 128 : 256;
+    if (N % tn256 != 0) return false;
+    const int ov = gemm_bn_override();
+    if (ov == 128 || ov == 256) return ov == 256;
+    const long long tiles_m = (M + BM - 1) / BM, sms = device_sms();
+    const long long r128 = (tiles_m * (N / tn128) + sms - 1) / sms, r256 = (tiles_m * (N / tn256) + sms - 1) / sms;
+    return 2.0 * WIDE_COST * (double)r256 < (double)r128;
+}
+
 }  // namespace
+
+int set_gemm_tile_width(int bn) {
+    const int prev = g_tile_width;
+    g_tile_width = bn;
+    return prev;
+}
 
 bool gemm_tc_supported(int N, int K, int mode, int lda) {
     if (K % BK != 0 || lda % 8 != 0) return false;
@@ -430,9 +477,17 @@ cudaError_t launch_gemm_tc(const bf16_t* A, int lda, const bf16_t* W, int M, int
     splits = (nkb + per - 1) / per;
     CUtensorMap ma, mb;
     const int w_rows = (mode == GEMM_SWIGLU_BF16) ? up_off + N : N;
+    const bool wide = mode != GEMM_ATOMIC_F32 && use_wide_tiles(M, N, mode);
     if (!make_map(&ma, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, BM)) return cudaErrorInvalidValue;
-    if (!make_map(&mb, W, (uint64_t)w_rows, (uint64_t)K, (uint64_t)K, mode == GEMM_SWIGLU_BF16 ? 64 : 128))
+    if (!make_map(&mb, W, (uint64_t)w_rows, (uint64_t)K, (uint64_t)K, (uint32_t)b_box_rows(wide ? 256 : 128, mode)))
         return cudaErrorInvalidValue;
+    if (wide) switch (mode) {
+        case GEMM_STORE_F32: return launch_bn<256, GEMM_STORE_F32, 4>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
+        case GEMM_ADD_F32: return launch_bn<256, GEMM_ADD_F32, 4>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
+        case GEMM_SWIGLU_BF16: return launch_bn<256, GEMM_SWIGLU_BF16, 4>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
+        case GEMM_STORE_BF16: return launch_bn<256, GEMM_STORE_BF16, 4>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
+        default: return cudaErrorInvalidValue;
+    }
     switch (mode) {
         case GEMM_STORE_F32: return launch_bn<128, GEMM_STORE_F32, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
         case GEMM_ADD_F32: return launch_bn<128, GEMM_ADD_F32, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
@@ -458,6 +513,8 @@ cudaError_t launch_gemm_tc_qkv_rope(const bf16_t* A, int lda, const bf16_t* W, i
     CUtensorMap ma, mb;
     if (!make_map(&ma, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, BM)) return cudaErrorInvalidValue;
     if (!make_map(&mb, W, (uint64_t)N, (uint64_t)K, (uint64_t)K, 128)) return cudaErrorInvalidValue;
+    if (use_wide_tiles(M, N, GEMM_QKV_ROPE))   // two heads per 256-column tile
+        return launch_bn<256, GEMM_QKV_ROPE, 4>(ma, mb, M, N, K, 0, nullptr, nullptr, 0, 1, s, epi);
     return launch_bn<128, GEMM_QKV_ROPE, 6>(ma, mb, M, N, K, 0, nullptr, nullptr, 0, 1, s, epi);
 }
 

@@ -47,6 +47,12 @@ int qdec_op_gemm_splitk(const void* A, int32_t lda, const void* W, int32_t M, in
                                       GEMM_ATOMIC_F32, 0, C, nullptr, ldc, static_cast<cudaStream_t>(stream), splits));
 }
 
+int qdec_op_gemm_tile_width(int32_t bn) {
+    if (bn != 0 && bn != 128 && bn != 256)
+        return set_error(QDEC_E_INVALID_ARG, "qdec_op_gemm_tile_width: %d is not 0, 128 or 256", bn);
+    return set_gemm_tile_width(bn);
+}
+
 int qdec_op_device_error(void) {
     const int v1 = tc_error_read_and_clear(), v2 = fa_error_read_and_clear();
     if (v1 < 0 || v2 < 0) return set_error(QDEC_E_CUDA, "reading the device error word failed");

@@ -58,11 +58,12 @@ def test_teacher_forced_workload(full, name):
     assert np.array_equal(hist[:wl.n_prompt][mask], kv_prompt[mask])
 
 
-@pytest.mark.parametrize("name", ["funasr_nano_short", "qwen3_asr_30s"])
-def test_fused_qkv_epilogue_matches_separate_kernels(full, name):
+@pytest.mark.parametrize("name,tile", [("funasr_nano_short", 0), ("qwen3_asr_30s", 0), ("qwen3_asr_30s", 256)])
+def test_fused_qkv_epilogue_matches_separate_kernels(full, name, tile):
     """The tcgen05 prefill writes K and V from the QKV GEMM's epilogue (per-head norm + RoPE
     fused); the CUDA-core prefill runs the GEMM and the norm/RoPE/append kernel separately.
-    Both caches and the prefill logits must agree to bf16 rounding."""
+    Both caches and the prefill logits must agree to bf16 rounding.  tile=256 forces the
+    128 x 256 GEMM tiles (two heads per tile) that long prompts use."""
     w, wd, orc = full
     wl = synth.WORKLOADS[name]
     p = synth.make_prompt(wl, seed=0)
@@ -71,7 +72,12 @@ def test_fused_qkv_epilogue_matches_separate_kernels(full, name):
         d = Decoder(SH, wd, max_seq=wl.n_prompt + 1)
         d.set_option(_lib.OPT_PREFILL_IMPL, impl)
         lg = torch.empty(SH.vocab, device="cuda")
-        d.prefill(p.ids, p.audio.cuda(), p.audio_offset, logits=lg)
+        prev = _lib.gemm_tile_width(tile)
+        try:
+            d.prefill(p.ids, p.audio.cuda(), p.audio_offset, logits=lg)
+            d.sync()
+        finally:
+            _lib.gemm_tile_width(prev)
         decs.append(d)
         logits.append(lg.cpu().numpy())
     for layer in (0, 13, SH.n_layers - 1):

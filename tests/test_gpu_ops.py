@@ -51,6 +51,41 @@ def test_gemm_epilogues(impl, M, N, K, mode):
     assert (got - ref).abs().max().item() <= tol
 
 
+WIDE_CASES = [(1, 256, 128), (130, 512, 384), (77, 4096, 1024), (300, 1024, 2048), (415, 1024, 3072)]
+
+
+@pytest.mark.parametrize("M,N,K", WIDE_CASES)
+@pytest.mark.parametrize("mode", [_lib.GEMM_STORE_F32, _lib.GEMM_ADD_F32, _lib.GEMM_SWIGLU_BF16, _lib.GEMM_STORE_BF16])
+def test_gemm_wide_tiles(M, N, K, mode):
+    """The tcgen05 GEMM with 128 x 256 tiles (SwiGLU: 128 gate + 128 up columns), forced."""
+    up_off = N + 128 if mode == _lib.GEMM_SWIGLU_BF16 else 0
+    rows = up_off + N if mode == _lib.GEMM_SWIGLU_BF16 else N
+    A = _bf16((M, K), 21, 0.5)
+    W = _bf16((rows, K), 22, 0.05)
+    bf = mode in (_lib.GEMM_SWIGLU_BF16, _lib.GEMM_STORE_BF16)
+    C0 = torch.zeros(M, N) if bf else _bf16((M, N), 23).float()
+    Cd = C0.to(torch.bfloat16).cuda() if bf else C0.cuda()
+    prev = _lib.gemm_tile_width(256)
+    try:
+        _lib.gemm(A.cuda(), W.cuda(), M, N, K, mode, Cd, up_off=up_off, impl=_lib.IMPL_TCGEN05)
+        torch.cuda.synchronize()
+    finally:
+        _lib.gemm_tile_width(prev)
+    _lib.device_error()
+    ref = _gemm_ref(A, W, mode, N, up_off)
+    if mode == _lib.GEMM_ADD_F32:
+        ref = ref + C0.double()
+    got = Cd.cpu().double()
+    tol = 8e-3 if bf else 2e-5
+    assert (got - ref).abs().max().item() <= tol * ref.abs().max().item() + 1e-6
+
+
+def test_gemm_tile_width_rejects_other_values():
+    with pytest.raises(_lib.QdecError):
+        _lib.gemm_tile_width(192)
+    assert _lib.gemm_tile_width(0) == 0
+
+
 @pytest.mark.parametrize("M,N,K,splits", [(64, 4096, 1024, 8), (64, 1024, 3072, 32), (5, 256, 128, 2),
                                           (64, 6144, 1024, 4), (130, 1024, 2048, 3)])
 def test_gemm_splitk_atomic(M, N, K, splits):
