@@ -366,12 +366,30 @@ __global__ void __launch_bounds__(192, 1) attn_prefill_tc_kernel(const __grid_co
 constexpr int NSLOT = 3;
 constexpr float LAZY_RESCALE_LOG2 = 8.f;
 
+// Two fp32 values to one bf16x2 word (lo in the low half), round to nearest even: one
+// conversion instruction per pair.
+__device__ __forceinline__ uint32_t pack_bf2x(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
 struct Fa2Bars {
     uint64_t q_full, ring_full[NSLOT], ring_empty[NSLOT], s_full[2], s_free[2], p_full[2], p_free[2], fin;
     uint32_t tmem;
     int abort;
 };
 
+// Non-blocking: has the phase of parity ph completed?
+__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t ph) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(s32(b)), "r"(ph)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ bool mb_wait_ab(uint64_t* b, uint32_t ph, int code, volatile int* abort) {
     for (uint32_t i = 0; i < FA_SPIN; ++i) {
         if (mb_try(b, ph)) return true;
@@ -489,54 +507,73 @@ __global__ void __launch_bounds__(320, 1) attn_prefill_tc2_kernel(const __grid_c
                 mb_wait(&B->ring_full[i % NSLOT], (i / NSLOT) & 1, 33);
         }
     } else if (warp == 1) {
-        if (lane == 0) {   // ---- MMA issuer
+        if (lane == 0) {   // ---- MMA issuer: issues whichever MMA of either head is ready
             constexpr uint32_t id_s = idesc_fa(false), id_o = idesc_fa(true);
-            uint32_t n = 0;
+            // ring item of K_j / V_j in the producer's order K0, K1, V0, K2, V1, ..., V_{nt-1}
+            auto kitem = [&](int j) { return j == 0 ? 0 : 2 * j - 1; };
+            auto vitem = [&](int j) { return j + 1 < nt ? 2 * j + 2 : 2 * nt - 1; };
+            auto ready = [&](uint64_t* bar, uint32_t ph) { return mbar_test(bar, ph); };
+            int js[2] = {0, 0}, jp[2] = {0, 0};   // next S and next P.V tile of each head
             bool ok = mb_wait_ab(&B->q_full, 0, 34, abort);
-            auto pv = [&](int i) {   // O(h) += P_i(h) V_i for both heads
-                const uint32_t slot = n % NSLOT;
-                if (!mb_wait_ab(&B->ring_full[slot], (n / NSLOT) & 1, 35, abort)) return false;
-                const char* v = sRing + slot * TILE_BYTES;
+            uint32_t idle = 0;
+            while (ok && (jp[0] < nt || jp[1] < nt)) {
+                bool issued = false;
+#pragma unroll 1
                 for (int hh = 0; hh < 2; ++hh) {
-                    if (!mb_wait_ab(&B->p_full[hh], i & 1, 36, abort)) return false;
-                    tc_fence_after();
-                    const char* pp = sP + hh * TILE_BYTES;
+                    // S_j(h) = Q_h K_j^T once K_j has landed and head h has read S_{j-1}(h)
+                    const int j = js[hh];
+                    if (j < nt) {
+                        const int it = kitem(j);
+                        const uint32_t slot = (uint32_t)it % NSLOT;
+                        if (ready(&B->ring_full[slot], ((uint32_t)it / NSLOT) & 1) &&
+                            (j == 0 || ready(&B->s_free[hh], (j - 1) & 1))) {
+                            tc_fence_after();
+                            const char* k = sRing + slot * TILE_BYTES;
+                            const char* qq = sQ + hh * TILE_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t ad = desc_kmajor(pp + (kk >> 2) * BLK) + 2 * (kk & 3);
-                        const uint64_t bd = desc_mnmajor(v) + (uint64_t)((kk * 16 * 128) >> 4);
-                        mma_bf16(tmem + 256 * hh + 128, ad, bd, id_o, (i > 0 || kk != 0) ? 1u : 0u);
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint64_t ad = desc_kmajor(qq + (kk >> 2) * BLK) + 2 * (kk & 3);
+                                const uint64_t bd = desc_kmajor(k + (kk >> 2) * BLK) + 2 * (kk & 3);
+                                mma_bf16(tmem + 256 * hh, ad, bd, id_s, kk != 0);
+                            }
+                            mma_commit(&B->s_full[hh]);
+                            if (js[hh ^ 1] > j) mma_commit(&B->ring_empty[slot]);   // both heads done with K_j
+                            js[hh] = j + 1;
+                            issued = true;
+                        }
                     }
-                    mma_commit(&B->p_free[hh]);
-                }
-                mma_commit(&B->ring_empty[slot]);
-                ++n;
-                return true;
-            };
-            for (int j = 0; j < nt && ok; ++j) {
-                const uint32_t slot = n % NSLOT;
-                ok = mb_wait_ab(&B->ring_full[slot], (n / NSLOT) & 1, 37, abort);
-                if (!ok) break;
-                const char* k = sRing + slot * TILE_BYTES;
-                for (int hh = 0; hh < 2 && ok; ++hh) {
-                    if (j >= 1) ok = mb_wait_ab(&B->s_free[hh], (j - 1) & 1, 38, abort);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const char* qq = sQ + hh * TILE_BYTES;
+                    // O(h) += P_i(h) V_i once P_i(h) is in shared memory and V_i has landed
+                    const int i = jp[hh];
+                    if (i < js[hh]) {
+                        const int it = vitem(i);
+                        const uint32_t slot = (uint32_t)it % NSLOT;
+                        if (ready(&B->ring_full[slot], ((uint32_t)it / NSLOT) & 1) && ready(&B->p_full[hh], i & 1)) {
+                            tc_fence_after();
+                            const char* v = sRing + slot * TILE_BYTES;
+                            const char* pp = sP + hh * TILE_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t ad = desc_kmajor(qq + (kk >> 2) * BLK) + 2 * (kk & 3);
-                        const uint64_t bd = desc_kmajor(k + (kk >> 2) * BLK) + 2 * (kk & 3);
-                        mma_bf16(tmem + 256 * hh, ad, bd, id_s, kk != 0);
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint64_t ad = desc_kmajor(pp + (kk >> 2) * BLK) + 2 * (kk & 3);
+                                const uint64_t bd = desc_mnmajor(v) + (uint64_t)((kk * 16 * 128) >> 4);
+                                mma_bf16(tmem + 256 * hh + 128, ad, bd, id_o, (i > 0 || kk != 0) ? 1u : 0u);
+                            }
+                            mma_commit(&B->p_free[hh]);
+                            if (jp[hh ^ 1] > i) mma_commit(&B->ring_empty[slot]);   // both heads done with V_i
+                            jp[hh] = i + 1;
+                            issued = true;
+                        }
                     }
-                    mma_commit(&B->s_full[hh]);
                 }
-                if (!ok) break;
-                mma_commit(&B->ring_empty[slot]);
-                ++n;
-                if (j >= 1) ok = pv(j - 1);
+                if (issued) {
+                    idle = 0;
+                } else if (++idle >= FA_SPIN) {
+                    *abort = 1;
+                    atomicCAS(&g_fa_error, 0, 35);
+                    ok = false;
+                } else if ((idle & 255) == 255 && *abort) {
+                    ok = false;
+                }
             }
-            if (ok && nt >= 1) pv(nt - 1);
             mma_commit(&B->fin);   // TMEM is freed only after every issued MMA has completed
             mb_wait(&B->fin, 0, 39);
         }
@@ -587,28 +624,50 @@ __global__ void __launch_bounds__(320, 1) attn_prefill_tc2_kernel(const __grid_c
                 corr = (m_run == -INFINITY) ? 0.f : ex2(m_run - m_tile);
                 m_run = m_tile;
             }
-            // P_j = exp2(s * c - m) (0 where masked), packed to bf16 pairs in place
-            float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+            // P_j = exp2(s * c - m) (0 where masked), in two halves of 64 keys: the arguments,
+            // then the exponentials, then the row sum and the bf16 pairs, each in bulk over
+            // independent values (a half's packed words free half of its registers)
             const bool live = m_run != -INFINITY;
+            const float nm = -m_run;
+            float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int hf = 0; hf < 2; ++hf) {
+                if (full) {
 #pragma unroll
-                for (int k = 0; k < 32; k += 2) {
-                    float p0, p1;
-                    if (full) {
-                        p0 = ex2(fmaf(__uint_as_float(sr[c][k]), scale_log2, -m_run));
-                        p1 = ex2(fmaf(__uint_as_float(sr[c][k + 1]), scale_log2, -m_run));
-                    } else {
-                        const int key = j * KT + 32 * c + k;
-                        p0 = (live && key <= qpos && key < L) ? ex2(fmaf(__uint_as_float(sr[c][k]), scale_log2, -m_run)) : 0.f;
-                        p1 = (live && key + 1 <= qpos && key + 1 < L)
-                                 ? ex2(fmaf(__uint_as_float(sr[c][k + 1]), scale_log2, -m_run))
-                                 : 0.f;
-                    }
-                    ls4[k & 3] += p0;
-                    ls4[(k + 1) & 3] += p1;
-                    sr[c][k >> 1] = pack_bf2(p0, p1);   // k >> 1 < k for k >= 2: never overwrites an unread value
+                    for (int c = 2 * hf; c < 2 * hf + 2; ++c)
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            sr[c][k] = __float_as_uint(fmaf(__uint_as_float(sr[c][k]), scale_log2, nm));
+                } else {
+#pragma unroll
+                    for (int c = 2 * hf; c < 2 * hf + 2; ++c)
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) {
+                            const int key = j * KT + 32 * c + k;
+                            const bool vis = live && key <= qpos && key < L;
+                            sr[c][k] = __float_as_uint(vis ? fmaf(__uint_as_float(sr[c][k]), scale_log2, nm) : -INFINITY);
+                        }
                 }
+#pragma unroll
+                for (int c = 2 * hf; c < 2 * hf + 2; ++c)
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) sr[c][k] = __float_as_uint(ex2(__uint_as_float(sr[c][k])));
+#pragma unroll
+                for (int c = 2 * hf; c < 2 * hf + 2; ++c)
+#pragma unroll
+                    for (int k = 0; k < 32; k += 4) {
+                        ls4[0] += __uint_as_float(sr[c][k]);
+                        ls4[1] += __uint_as_float(sr[c][k + 1]);
+                        ls4[2] += __uint_as_float(sr[c][k + 2]);
+                        ls4[3] += __uint_as_float(sr[c][k + 3]);
+                    }
+                // pairs packed in place: word k/2 of chunk c holds keys 32c + k, 32c + k + 1
+#pragma unroll
+                for (int c = 2 * hf; c < 2 * hf + 2; ++c)
+#pragma unroll
+                    for (int k = 0; k < 32; k += 2)
+                        sr[c][k >> 1] = pack_bf2x(__uint_as_float(sr[c][k]), __uint_as_float(sr[c][k + 1]));
+            }
             l = l * corr + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
             if (j >= 1) {   // P(h) and O(h) are free once P_{j-1}(h) V_{j-1} has completed
                 if (!__all_sync(0xffffffffu, mb_wait_ab(&B->p_free[hh], (j - 1) & 1, 41, abort))) {
