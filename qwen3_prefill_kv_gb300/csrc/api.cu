@@ -146,6 +146,8 @@ struct qdec_ctx {
     // prefill scratch (grown on demand)
     int pf_cap = 0;
     float *p_X = nullptr, *p_qkv = nullptr;
+    float* p_part = nullptr;     // split-K partial slabs of the short-prompt prefill GEMMs
+    size_t part_cap = 0;         // floats
     bf16_t *p_Xn = nullptr, *p_Q = nullptr, *p_O = nullptr, *p_H = nullptr;
     int* p_ids = nullptr;
     int audio_cap = 0;
@@ -195,7 +197,7 @@ void free_all(qdec_ctx* c) {
     if (c->decode_exec) cudaGraphExecDestroy(c->decode_exec);
     void* ptrs[] = {c->kv, c->rope, c->d_hist, c->d_pos, c->d_zero, c->d_argmax, c->d_x, c->d_qkv, c->d_q,
                     c->d_attn, c->d_h, c->d_logits, c->d_part_ml, c->d_part_o, c->d_lm_scratch, c->p_X,
-                    c->p_qkv, c->p_Xn, c->p_Q, c->p_O, c->p_H, c->p_ids, c->p_audio, c->d_layers, c->ll_x,
+                    c->p_qkv, c->p_Xn, c->p_Q, c->p_O, c->p_H, c->p_ids, c->p_audio, c->p_part, c->d_layers, c->ll_x,
                     c->ll_qkv, c->ll_o, c->ll_h, c->attn_part, c->attn_count, c->am_part, c->am_count,
                     c->d_trace};
     for (void* p : ptrs)
@@ -313,6 +315,13 @@ int build_rope_table(qdec_ctx* c) {
 }
 
 int ensure_prefill_scratch(qdec_ctx* c, int T) {
+    if (!c->p_part && c->prefill_gemm == QDEC_PREFILL_TCGEN05) {
+        // partial slabs of a split GEMM: splits * M * N <= (SMs + tiles) * 128 * 128 with
+        // tiles <= SMs / 2 (prefill_splits)
+        const size_t cap = (size_t)2 * c->sms * 128 * 128;
+        CK(dalloc(&c->p_part, cap));
+        c->part_cap = cap;
+    }
     if (T <= c->pf_cap) return QDEC_OK;
     const Shape& sh = c->sh;
     void* old[] = {c->p_X, c->p_qkv, c->p_Xn, c->p_Q, c->p_O, c->p_H, c->p_ids};
@@ -352,8 +361,6 @@ int copy_logits_out(qdec_ctx* c, float* dst) {
     return QDEC_OK;
 }
 
-constexpr uint64_t kPrefillKernelsPerLayer = 7;   // + 1 when the QKV epilogue is not fused
-
 // Prefill GEMM: tcgen05 kernel where the shape allows it (and it is selected), else CUDA cores.
 cudaError_t prefill_gemm(const qdec_ctx* c, const bf16_t* A, int lda, const bf16_t* W, int M, int N, int K, int mode,
                          int up_off, float* Cf, bf16_t* Cb, int ldc, cudaStream_t s) {
@@ -362,32 +369,84 @@ cudaError_t prefill_gemm(const qdec_ctx* c, const bf16_t* A, int lda, const bf16
     return launch_gemm_simt(A, lda, W, M, N, K, mode, up_off, Cf, Cb, ldc, s);
 }
 
-// One layer of the prefill over T rows starting at position 0.
-int prefill_layer(qdec_ctx* c, int l, int T) {
+// Split-K factor of a prefill GEMM on the tensor cores.  A short prompt has few 128 x 128
+// output tiles (64 rows and o_proj's 1024 columns: 8 tiles for 152 SMs), so each tile's K is
+// split over enough CTAs to fill the SMs once; split z stores an fp32 partial slab and the
+// kernel that consumes the product adds the slabs in order (deterministic).  1 = no split.
+int prefill_splits(const qdec_ctx* c, int M, int N, int K, int lda) {
+    if (c->prefill_gemm != QDEC_PREFILL_TCGEN05 || !gemm_tc_supported(N, K, GEMM_PARTIAL_F32, lda)) return 1;
+    const int tiles = ((M + 127) / 128) * (N / 128);
+    if (2 * tiles > c->sms) return 1;
+    const int sp = gemm_tc_splits(K, (c->sms + tiles - 1) / tiles);
+    if ((size_t)sp * M * N > c->part_cap) return 1;
+    return sp;
+}
+
+// One layer of the prefill over T rows starting at position 0.  *fold carries split-K
+// partials of the previous down projection still to be added into the residual (0 = none);
+// *kernels counts the launches.
+int prefill_layer(qdec_ctx* c, int l, int T, int* fold, uint64_t* kernels) {
     const Shape& sh = c->sh;
     const LayerW& w = c->layers[l];
     cudaStream_t s = c->stream;
-    const int qd = sh.HQ * sh.D;
-    CK(launch_rmsnorm_bf16(c->p_X, T, sh.H, w.g_in, sh.eps, c->p_Xn, s));
-    if (c->prefill_gemm == QDEC_PREFILL_TCGEN05 && gemm_tc_qkv_rope_supported(sh, sh.H)) {
+    const int qd = sh.HQ * sh.D, nq = sh.qkv_rows();
+    uint64_t k = 0;
+    if (*fold > 1)
+        CK(launch_rmsnorm_fold_bf16(c->p_X, c->p_part, *fold, (size_t)T * sh.H, T, sh.H, w.g_in, sh.eps, c->p_Xn, s));
+    else
+        CK(launch_rmsnorm_bf16(c->p_X, T, sh.H, w.g_in, sh.eps, c->p_Xn, s));
+    *fold = 0;
+    ++k;
+    const int sq = prefill_splits(c, T, nq, sh.H, sh.H);
+    if (sq > 1) {
+        CK(launch_gemm_tc(c->p_Xn, sh.H, w.wqkv, T, nq, sh.H, GEMM_PARTIAL_F32, 0, c->p_part, nullptr, nq, s, sq));
+        CK(launch_qk_norm_rope_append(c->p_part, T, sh, c->d_zero, w.g_q, w.g_k, c->rope, c->p_Q, nullptr,
+                                      c->k_cache(l), c->v_cache(l), s, sq, (size_t)T * nq));
+        k += 2;
+    } else if (c->prefill_gemm == QDEC_PREFILL_TCGEN05 && gemm_tc_qkv_rope_supported(sh, sh.H)) {
         // QKV projection with the per-head norm, RoPE and KV append in its epilogue
         QkvRopeEpi e{c->rope, w.g_q, w.g_k, c->p_Q, c->k_cache(l), c->v_cache(l), 0, sh.HQ, sh.HKV, sh.max_seq, sh.eps};
         CK(launch_gemm_tc_qkv_rope(c->p_Xn, sh.H, w.wqkv, T, sh.H, e, s));
+        k += 1;
     } else {
-        CK(prefill_gemm(c, c->p_Xn, sh.H, w.wqkv, T, sh.qkv_rows(), sh.H, GEMM_STORE_F32, 0, c->p_qkv, nullptr,
-                        sh.qkv_rows(), s));
+        CK(prefill_gemm(c, c->p_Xn, sh.H, w.wqkv, T, nq, sh.H, GEMM_STORE_F32, 0, c->p_qkv, nullptr, nq, s));
         CK(launch_qk_norm_rope_append(c->p_qkv, T, sh, c->d_zero, w.g_q, w.g_k, c->rope, c->p_Q, nullptr,
                                       c->k_cache(l), c->v_cache(l), s));
-        count_launches(1);
+        k += 2;
     }
     if (c->prefill_gemm == QDEC_PREFILL_TCGEN05 && attention_tc_supported(sh))
         CK(launch_attention_prefill_tc(c->p_Q, T, sh, 0, c->k_cache(l), c->v_cache(l), c->p_O, s));
     else
         CK(launch_attention_prefill_simt(c->p_Q, T, sh, 0, c->k_cache(l), c->v_cache(l), c->p_O, s));
-    CK(prefill_gemm(c, c->p_O, qd, w.wo, T, sh.H, qd, GEMM_ADD_F32, 0, c->p_X, nullptr, sh.H, s));
-    CK(launch_rmsnorm_bf16(c->p_X, T, sh.H, w.g_post, sh.eps, c->p_Xn, s));
-    CK(prefill_gemm(c, c->p_Xn, sh.H, w.wgu, T, sh.F, sh.H, GEMM_SWIGLU_BF16, sh.F, nullptr, c->p_H, sh.F, s));
-    CK(prefill_gemm(c, c->p_H, sh.F, w.wd, T, sh.H, sh.F, GEMM_ADD_F32, 0, c->p_X, nullptr, sh.H, s));
+    ++k;
+    const int so = prefill_splits(c, T, sh.H, qd, qd);
+    if (so > 1) {   // o_proj partials, added into the residual by the post-attention norm
+        CK(launch_gemm_tc(c->p_O, qd, w.wo, T, sh.H, qd, GEMM_PARTIAL_F32, 0, c->p_part, nullptr, sh.H, s, so));
+        CK(launch_rmsnorm_fold_bf16(c->p_X, c->p_part, so, (size_t)T * sh.H, T, sh.H, w.g_post, sh.eps, c->p_Xn, s));
+    } else {
+        CK(prefill_gemm(c, c->p_O, qd, w.wo, T, sh.H, qd, GEMM_ADD_F32, 0, c->p_X, nullptr, sh.H, s));
+        CK(launch_rmsnorm_bf16(c->p_X, T, sh.H, w.g_post, sh.eps, c->p_Xn, s));
+    }
+    k += 2;
+    const int sg = prefill_splits(c, T, 2 * sh.F, sh.H, sh.H);
+    if (sg > 1) {   // gate and up partials, summed by the SwiGLU kernel
+        CK(launch_gemm_tc(c->p_Xn, sh.H, w.wgu, T, 2 * sh.F, sh.H, GEMM_PARTIAL_F32, 0, c->p_part, nullptr, 2 * sh.F,
+                          s, sg));
+        CK(launch_batch_swiglu(c->p_part, sh.F, T, c->p_H, s, sg, (size_t)T * 2 * sh.F));
+        k += 2;
+    } else {
+        CK(prefill_gemm(c, c->p_Xn, sh.H, w.wgu, T, sh.F, sh.H, GEMM_SWIGLU_BF16, sh.F, nullptr, c->p_H, sh.F, s));
+        k += 1;
+    }
+    const int sd = prefill_splits(c, T, sh.H, sh.F, sh.F);
+    if (sd > 1) {   // down partials: added by the next layer's norm (or after the last layer)
+        CK(launch_gemm_tc(c->p_H, sh.F, w.wd, T, sh.H, sh.F, GEMM_PARTIAL_F32, 0, c->p_part, nullptr, sh.H, s, sd));
+        *fold = sd;
+    } else {
+        CK(prefill_gemm(c, c->p_H, sh.F, w.wd, T, sh.H, sh.F, GEMM_ADD_F32, 0, c->p_X, nullptr, sh.H, s));
+    }
+    k += 1;
+    *kernels += k;
     return QDEC_OK;
 }
 
@@ -771,14 +830,21 @@ int qdec_prefill(qdec_ctx* c, const int32_t* ids, int32_t n_ids, const void* aud
     c->prefilled = false;
     c->position = 0;
     CK(launch_embed_splice(c->embed, c->p_ids, T, sh.H, audio, n_audio, audio_offset, c->p_X, c->d_hist, s));
+    uint64_t kernels = 3;   // embed, lm_head, position
+    int fold = 0;
     for (int l = 0; l < sh.NL; ++l) {
-        rc = prefill_layer(c, l, T);
+        rc = prefill_layer(c, l, T, &fold, &kernels);
         if (rc != QDEC_OK) return rc;
+    }
+    if (fold > 1) {   // the last down projection's partials, for the row the head reads
+        const size_t last = (size_t)(T - 1) * sh.H;
+        CK(launch_fold_partials(c->p_X + last, c->p_part + last, fold, (size_t)T * sh.H, (size_t)sh.H, s));
+        ++kernels;
     }
     CK(launch_lm_head_argmax(c->embed, sh.V, sh.H, c->p_X + (size_t)(T - 1) * sh.H, c->final_norm, sh.eps,
                              c->d_logits, c->d_argmax, c->d_lm_scratch, s));
     CK(launch_set_int(c->d_pos, T, s));
-    count_launches(3 + (uint64_t)sh.NL * kPrefillKernelsPerLayer);
+    count_launches(kernels);
     c->position = T;
     c->prefilled = true;
     rc = copy_logits_out(c, logits_out);

@@ -64,9 +64,17 @@ int set_error(int code, const char* fmt, ...);
 // out[t] = bf16(X[t] * rsqrt(mean X[t]^2 + eps) * g)
 cudaError_t launch_rmsnorm_bf16(const float* X, int T, int H, const bf16_t* g, float eps,
                                 bf16_t* out, cudaStream_t s);
+// The same after X[t] += sum_z part[z * pstride + t * H] (z = 0 .. splits-1 in order; X is
+// updated in place): the residual add of a split-K projection folded into the next norm.
+cudaError_t launch_rmsnorm_fold_bf16(float* X, const float* part, int splits, size_t pstride, int T, int H,
+                                     const bf16_t* g, float eps, bf16_t* out, cudaStream_t s);
+// X[i] += sum_z part[z * pstride + i] for i < n (fixed order).
+cudaError_t launch_fold_partials(float* X, const float* part, int splits, size_t pstride, size_t n, cudaStream_t s);
 
 enum GemmMode { GEMM_STORE_F32 = 0, GEMM_ADD_F32 = 1, GEMM_SWIGLU_BF16 = 2, GEMM_STORE_BF16 = 3, GEMM_ATOMIC_F32 = 4,
-                GEMM_QKV_ROPE = 5 };
+                GEMM_QKV_ROPE = 5, GEMM_PARTIAL_F32 = 6 };
+// GEMM_PARTIAL_F32 splits K over `splits` CTAs per tile; split z stores its fp32 partial to
+// C + z * M * ldc (plain stores, no atomics): the consumer adds the slabs in a fixed order.
 // C[M, N] (op) A[M, K] . W[N, K]^T.  SWIGLU: W is [2N, K] (gate rows, then up rows at
 // offset `up_off` rows) and C_bf16[m, n] = silu(gate) * up.
 cudaError_t launch_gemm_simt(const bf16_t* A, int lda, const bf16_t* W, int M, int N, int K, int mode,
@@ -75,7 +83,10 @@ cudaError_t launch_gemm_simt(const bf16_t* A, int lda, const bf16_t* W, int M, i
 // The same GEMM on the tcgen05 tensor cores (TMA-fed, TMEM accumulator).  Needs K % 64 == 0,
 // lda % 8 == 0, N % 128 == 0 (SwiGLU: N % 64 == 0) and 16-byte aligned A, W.
 bool gemm_tc_supported(int N, int K, int mode, int lda);
-// GEMM_ATOMIC_F32 (C += acc with fp32 vector atomics) may split K over `splits` CTAs per tile.
+// GEMM_ATOMIC_F32 (C += acc with fp32 vector atomics) and GEMM_PARTIAL_F32 may split K over
+// `splits` CTAs per tile.  gemm_tc_splits() gives the count the launcher actually uses (every
+// split gets at least one 64-wide k-block).
+int gemm_tc_splits(int K, int splits);
 // Forces the tcgen05 GEMM's tile width (128 or 256; 0 = chosen per shape); returns the previous
 // setting.  Process-wide, not thread-safe: for tuning and tests.
 int set_gemm_tile_width(int bn);
@@ -100,10 +111,11 @@ int tc_error_read_and_clear();
 
 // Per-head RMSNorm + NeoX RoPE on q and k, V copy, KV append at slots pos0 + t.
 // qkv fp32 [T, (HQ+2HKV) D]; q_out: bf16 [T, HQ, D] (q_bf16) or fp32 (q_f32).
+// qkv may be the first of `splits` split-K partial slabs pstride floats apart (summed in order).
 cudaError_t launch_qk_norm_rope_append(const float* qkv, int T, const Shape& sh, const int* pos0,
                                        const bf16_t* g_q, const bf16_t* g_k, const float2* rope_cs,
                                        bf16_t* q_bf16, float* q_f32, bf16_t* k_cache, bf16_t* v_cache,
-                                       cudaStream_t s);
+                                       cudaStream_t s, int splits = 1, size_t pstride = 0);
 
 // Prefill attention: Q bf16 [T, HQ, D] at positions pos0..pos0+T-1 over cache keys [0, pos0+T).
 cudaError_t launch_attention_prefill_simt(const bf16_t* Q, int T, const Shape& sh, int pos0,
@@ -151,7 +163,10 @@ cudaError_t launch_batch_qk_rope(const float* qkv, const Shape& sh, int layer, c
                                  const BatchStream* bs, int n, float* q_out, cudaStream_t st);
 cudaError_t launch_batch_attention(const float* q, const Shape& sh, int layer, const BatchStream* bs, int n, int n_split,
                                    float* part_ml, float* part_o, bf16_t* out, cudaStream_t st);
-cudaError_t launch_batch_swiglu(const float* gu, int F, int n, bf16_t* h, cudaStream_t st);
+// h = silu(g) * u from gu [n, 2F] (gate, then up), or from the sum of `splits` partial slabs of
+// it pstride floats apart.
+cudaError_t launch_batch_swiglu(const float* gu, int F, int n, bf16_t* h, cudaStream_t st, int splits = 1,
+                                size_t pstride = 0);
 cudaError_t launch_batch_argmax(const float* logits, int V, int ld, const BatchStream* bs, int n, int* out,
                                 cudaStream_t st);
 

@@ -235,13 +235,19 @@ __global__ void batch_attn_merge_kernel(int HQ, int D, int n_split, const float*
 
 // h = silu(gate) * up from the fp32 [n, 2F] projection (gate columns first), bf16 [n, F].
 // One thread per pair of columns (F even) over all n rows.
-__global__ void batch_swiglu_kernel(const float* __restrict__ gu, int F, int n, bf16_t* __restrict__ h) {
+__global__ void batch_swiglu_kernel(const float* __restrict__ gu, int F, int n, bf16_t* __restrict__ h, int splits,
+                                    size_t pstride) {
     const int idx = blockIdx.x * blockDim.x + threadIdx.x;   // pair index
     const int half = F >> 1;
     if (idx >= n * half) return;
     const int s = idx / half, j = 2 * (idx - s * half);
-    const float2 g = *reinterpret_cast<const float2*>(gu + (size_t)s * 2 * F + j);
-    const float2 u = *reinterpret_cast<const float2*>(gu + (size_t)s * 2 * F + F + j);
+    float2 g = *reinterpret_cast<const float2*>(gu + (size_t)s * 2 * F + j);
+    float2 u = *reinterpret_cast<const float2*>(gu + (size_t)s * 2 * F + F + j);
+    for (int z = 1; z < splits; ++z) {   // split-K partial slabs, added in order
+        const float2 g2 = *reinterpret_cast<const float2*>(gu + z * pstride + (size_t)s * 2 * F + j);
+        const float2 u2 = *reinterpret_cast<const float2*>(gu + z * pstride + (size_t)s * 2 * F + F + j);
+        g.x += g2.x; g.y += g2.y; u.x += u2.x; u.y += u2.y;
+    }
     *reinterpret_cast<uint32_t*>(h + (size_t)s * F + j) = pack_bf2(silu(g.x) * u.x, silu(g.y) * u.y);
 }
 
@@ -336,11 +342,11 @@ cudaError_t launch_batch_attention(const float* q, const Shape& sh, int layer, c
     return cudaGetLastError();
 }
 
-cudaError_t launch_batch_swiglu(const float* gu, int F, int n, bf16_t* h, cudaStream_t st) {
+cudaError_t launch_batch_swiglu(const float* gu, int F, int n, bf16_t* h, cudaStream_t st, int splits, size_t pstride) {
     (void)cudaGetLastError();
-    if (F % 2 != 0) return cudaErrorInvalidValue;
+    if (F % 2 != 0 || splits < 1 || pstride % 2 != 0) return cudaErrorInvalidValue;
     const int pairs = n * (F / 2);
-    batch_swiglu_kernel<<<(pairs + 255) / 256, 256, 0, st>>>(gu, F, n, h);
+    batch_swiglu_kernel<<<(pairs + 255) / 256, 256, 0, st>>>(gu, F, n, h, splits, pstride);
     return cudaGetLastError();
 }
 

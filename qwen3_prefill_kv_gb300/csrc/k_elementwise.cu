@@ -109,13 +109,68 @@ cudaError_t launch_rmsnorm_bf16(const float* X, int T, int H, const bf16_t* g, f
     return cudaGetLastError();
 }
 
+// rmsnorm_bf16_kernel after folding split-K partials into the residual row: each thread
+// updates the elements it later normalises, so its own writes are what it reads back.
+__global__ void rmsnorm_fold_bf16_kernel(float* __restrict__ X, const float* __restrict__ part, int splits,
+                                         size_t pstride, int H, const bf16_t* __restrict__ g, float eps,
+                                         bf16_t* __restrict__ out) {
+    __shared__ float red[8];
+    float* x = X + (size_t)blockIdx.x * H;
+    const float* pr = part + (size_t)blockIdx.x * H;
+    float ss = 0.f;
+    for (int i = threadIdx.x * 4; i < H; i += 1024) {
+        float4 v = *reinterpret_cast<const float4*>(x + i);
+        for (int z = 0; z < splits; ++z) {
+            const float4 d = *reinterpret_cast<const float4*>(pr + z * pstride + i);
+            v.x += d.x; v.y += d.y; v.z += d.z; v.w += d.w;
+        }
+        *reinterpret_cast<float4*>(x + i) = v;
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+    ss = block_sum_256(ss, red);
+    const float r = rsqrtf(ss / (float)H + eps);
+    bf16_t* o = out + (size_t)blockIdx.x * H;
+    for (int i = threadIdx.x * 4; i < H; i += 1024) {
+        float4 v = *reinterpret_cast<const float4*>(x + i);
+        uint2 gw = *reinterpret_cast<const uint2*>(g + i);
+        uint2 ow;
+        ow.x = pack_bf2(v.x * r * bf_lo(gw.x), v.y * r * bf_hi(gw.x));
+        ow.y = pack_bf2(v.z * r * bf_lo(gw.y), v.w * r * bf_hi(gw.y));
+        *reinterpret_cast<uint2*>(o + i) = ow;
+    }
+}
+
+cudaError_t launch_rmsnorm_fold_bf16(float* X, const float* part, int splits, size_t pstride, int T, int H,
+                                     const bf16_t* g, float eps, bf16_t* out, cudaStream_t s) {
+    (void)cudaGetLastError();   // attribute only this launch's errors
+    if (H % 4 != 0 || pstride % 4 != 0 || splits < 1) return cudaErrorInvalidValue;
+    rmsnorm_fold_bf16_kernel<<<T, 256, 0, s>>>(X, part, splits, pstride, H, g, eps, out);
+    return cudaGetLastError();
+}
+
+__global__ void fold_partials_kernel(float* __restrict__ X, const float* __restrict__ part, int splits,
+                                     size_t pstride, size_t n) {
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    float v = X[i];
+    for (int z = 0; z < splits; ++z) v += part[z * pstride + i];
+    X[i] = v;
+}
+
+cudaError_t launch_fold_partials(float* X, const float* part, int splits, size_t pstride, size_t n, cudaStream_t s) {
+    (void)cudaGetLastError();   // attribute only this launch's errors
+    fold_partials_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(X, part, splits, pstride, n);
+    return cudaGetLastError();
+}
+
 // grid (T, HQ + 2 HKV), block max(32, D/2): thread i < D/2 owns the NeoX pair (i, i + D/2) of one head.
 __global__ void qk_norm_rope_append_kernel(const float* __restrict__ qkv, int HQ, int HKV, int D, int max_seq,
                                            float eps, const int* __restrict__ pos0,
                                            const bf16_t* __restrict__ g_q, const bf16_t* __restrict__ g_k,
                                            const float2* __restrict__ rope_cs,
                                            bf16_t* __restrict__ q_bf16, float* __restrict__ q_f32,
-                                           bf16_t* __restrict__ k_cache, bf16_t* __restrict__ v_cache) {
+                                           bf16_t* __restrict__ k_cache, bf16_t* __restrict__ v_cache,
+                                           int splits, size_t pstride) {
     __shared__ float red[4];
     const int t = blockIdx.x, hh = blockIdx.y, i = threadIdx.x, half = D >> 1;
     const int rows = (HQ + 2 * HKV) * D;
@@ -123,6 +178,11 @@ __global__ void qk_norm_rope_append_kernel(const float* __restrict__ qkv, int HQ
     const bool act = i < half;   // the block is padded to a whole warp when D/2 < 32
     const float* src = qkv + (size_t)t * rows + (size_t)hh * D;
     float a = act ? src[i] : 0.f, b = act ? src[i + half] : 0.f;
+    for (int z = 1; z < splits; ++z)   // split-K partial slabs, added in order
+        if (act) {
+            a += src[z * pstride + i];
+            b += src[z * pstride + i + half];
+        }
     if (hh >= HQ + HKV) {  // value head: plain copy into the cache
         const int g = hh - HQ - HKV;
         bf16_t* dst = v_cache + ((size_t)g * max_seq + p) * D;
@@ -168,11 +228,13 @@ __global__ void qk_norm_rope_append_kernel(const float* __restrict__ qkv, int HQ
 cudaError_t launch_qk_norm_rope_append(const float* qkv, int T, const Shape& sh, const int* pos0,
                                        const bf16_t* g_q, const bf16_t* g_k, const float2* rope_cs,
                                        bf16_t* q_bf16, float* q_f32, bf16_t* k_cache, bf16_t* v_cache,
-                                       cudaStream_t s) {
+                                       cudaStream_t s, int splits, size_t pstride) {
     (void)cudaGetLastError();   // attribute only this launch's errors
+    if (splits < 1) return cudaErrorInvalidValue;
     dim3 grid(T, sh.HQ + 2 * sh.HKV);
     qk_norm_rope_append_kernel<<<grid, sh.D / 2 < 32 ? 32 : sh.D / 2, 0, s>>>(qkv, sh.HQ, sh.HKV, sh.D, sh.max_seq, sh.eps, pos0,
-                                                         g_q, g_k, rope_cs, q_bf16, q_f32, k_cache, v_cache);
+                                                         g_q, g_k, rope_cs, q_bf16, q_f32, k_cache, v_cache,
+                                                         splits, pstride);
     return cudaGetLastError();
 }
 

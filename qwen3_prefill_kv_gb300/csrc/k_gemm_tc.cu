@@ -192,8 +192,9 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
     // same time share the weight (B) tile through L2; split z covers k-blocks [kb0, kb0 + nk)
     const int nkb = K / BK, per = (nkb + splits - 1) / splits;
     const int tiles = tiles_m * tiles_n, units = tiles * splits;
-    auto unit = [&](int u, int& m0, int& nt, int& kb0, int& nk) {
-        const int z = u / tiles, t = u - z * tiles;
+    auto unit = [&](int u, int& m0, int& nt, int& kb0, int& nk, int& z) {
+        z = u / tiles;
+        const int t = u - z * tiles;
         m0 = (t % tiles_m) * BM;
         nt = t / tiles_m;
         kb0 = z * per;
@@ -224,8 +225,8 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
             uint32_t g = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-                int m0, nt, kb0, nk;
-                unit(u, m0, nt, kb0, nk);
+                int m0, nt, kb0, nk, z;
+                unit(u, m0, nt, kb0, nk, z);
                 const int n0 = nt * (GLU ? BN / 2 : BN);
                 for (int kb = 0; kb < nk; ++kb, ++g) {
                     const uint32_t s = g % STAGES, r = g / STAGES;
@@ -255,8 +256,8 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
             bool ok = true;
             int j = 0;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++j) {
-                int m0, nt, kb0, nk;
-                unit(u, m0, nt, kb0, nk);
+                int m0, nt, kb0, nk, z;
+                unit(u, m0, nt, kb0, nk, z);
                 const int buf = j & 1;
                 if (!mb_wait_ab(&acc_empty[buf], ((j >> 1) & 1) ^ 1, 5, abort)) break;
                 tc_fence_after();
@@ -283,8 +284,8 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
         const int q = warp & 3;
         int j = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
-            int m0, nt, kb0, nk;
-            unit(u, m0, nt, kb0, nk);
+            int m0, nt, kb0, nk, z;
+            unit(u, m0, nt, kb0, nk, z);
             const int buf = j & 1;
             if (!mb_wait_ab(&acc_full[buf], (j >> 1) & 1, 3, abort)) break;
             tc_fence_after();
@@ -338,7 +339,9 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
                                 dst[jj] = make_uint4(pack_bf2(v[8 * jj], v[8 * jj + 1]), pack_bf2(v[8 * jj + 2], v[8 * jj + 3]),
                                                      pack_bf2(v[8 * jj + 4], v[8 * jj + 5]), pack_bf2(v[8 * jj + 6], v[8 * jj + 7]));
                         } else {
-                            float4* dst = reinterpret_cast<float4*>(Cf + (size_t)row * ldc + n0 + c0);
+                            // split-K partials go to slab z of M rows
+                            float* cbase = MODE == GEMM_PARTIAL_F32 ? Cf + (size_t)z * M * ldc : Cf;
+                            float4* dst = reinterpret_cast<float4*>(cbase + (size_t)row * ldc + n0 + c0);
 #pragma unroll
                             for (int jj = 0; jj < 8; ++jj) {
                                 float4 o = make_float4(v[4 * jj], v[4 * jj + 1], v[4 * jj + 2], v[4 * jj + 3]);
@@ -453,6 +456,14 @@ bool use_wide_tiles(int M, int N, int mode) {
 
 }  // namespace
 
+int gemm_tc_splits(int K, int splits) {
+    const int nkb = K / BK;
+    if (splits > nkb) splits = nkb;
+    if (splits < 1) splits = 1;
+    const int per = (nkb + splits - 1) / splits;
+    return (nkb + per - 1) / per;
+}
+
 int set_gemm_tile_width(int bn) {
     const int prev = g_tile_width;
     g_tile_width = bn;
@@ -469,15 +480,12 @@ cudaError_t launch_gemm_tc(const bf16_t* A, int lda, const bf16_t* W, int M, int
                            float* Cf, bf16_t* Cb, int ldc, cudaStream_t s, int splits) {
     (void)cudaGetLastError();
     if (!gemm_tc_supported(N, K, mode, lda) || M <= 0) return cudaErrorInvalidValue;
-    // each split needs at least one k-block; only the atomic mode may be split
-    const int nkb = K / BK;
-    if (splits < 1 || (splits > 1 && mode != GEMM_ATOMIC_F32)) return cudaErrorInvalidValue;
-    if (splits > nkb) splits = nkb;
-    const int per = (nkb + splits - 1) / splits;
-    splits = (nkb + per - 1) / per;
+    // each split needs at least one k-block; only the atomic and partial modes may be split
+    if (splits < 1 || (splits > 1 && mode != GEMM_ATOMIC_F32 && mode != GEMM_PARTIAL_F32)) return cudaErrorInvalidValue;
+    splits = gemm_tc_splits(K, splits);
     CUtensorMap ma, mb;
     const int w_rows = (mode == GEMM_SWIGLU_BF16) ? up_off + N : N;
-    const bool wide = mode != GEMM_ATOMIC_F32 && use_wide_tiles(M, N, mode);
+    const bool wide = mode != GEMM_ATOMIC_F32 && mode != GEMM_PARTIAL_F32 && use_wide_tiles(M, N, mode);
     if (!make_map(&ma, A, (uint64_t)M, (uint64_t)K, (uint64_t)lda, BM)) return cudaErrorInvalidValue;
     if (!make_map(&mb, W, (uint64_t)w_rows, (uint64_t)K, (uint64_t)K, (uint32_t)b_box_rows(wide ? 256 : 128, mode)))
         return cudaErrorInvalidValue;
@@ -495,6 +503,7 @@ cudaError_t launch_gemm_tc(const bf16_t* A, int lda, const bf16_t* W, int M, int
         case GEMM_STORE_BF16: return launch_bn<128, GEMM_STORE_BF16, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
         // split-K CTAs run few k-blocks each: a 3-stage ring (97 KB) lets two share an SM
         case GEMM_ATOMIC_F32: return launch_bn<128, GEMM_ATOMIC_F32, 3>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
+        case GEMM_PARTIAL_F32: return launch_bn<128, GEMM_PARTIAL_F32, 3>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
         default: return cudaErrorInvalidValue;
     }
 }
