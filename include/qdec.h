@@ -155,6 +155,12 @@ int qdec_sync(const qdec_ctx *ctx);
 #define QDEC_PREFILL_TCGEN05     0   /*   tcgen05 tensor cores, TMA-fed (default, where the shape
                                             allows: attention needs head_dim 128) */
 #define QDEC_PREFILL_SIMT        1   /*   CUDA cores */
+#define QDEC_OPT_ATTN_UNIT_KEYS  4   /* keys per attention unit of the persistent decode step
+                                        (the KV history is split into units of about this many
+                                        positions, at most one unit per SM; the last unit of a
+                                        kv head merges them): 0 = the library default (one unit
+                                        up to 160 keys, else about 64 keys per unit), or
+                                        8 .. 4096 in multiples of 8 */
 
 /* Sets an option.  QDEC_OPT_DECODE_KERNEL = QDEC_DECODE_PERSISTENT returns
  * UNSUPPORTED when the persistent kernel does not cover the shape (head_dim /

@@ -23,6 +23,7 @@ GEMM_STORE_F32, GEMM_ADD_F32, GEMM_SWIGLU_BF16, GEMM_STORE_BF16, GEMM_ATOMIC_F32
 OPT_DECODE_KERNEL = 1
 OPT_TRACE = 2
 OPT_PREFILL_IMPL = 3
+OPT_ATTN_UNIT_KEYS = 4
 PREFILL_TCGEN05, PREFILL_SIMT = 0, 1
 DECODE_PERSISTENT, DECODE_GRAPH = 0, 1
 IMPL_SIMT, IMPL_TCGEN05 = 0, 1

@@ -173,6 +173,7 @@ struct qdec_ctx {
     int* d_err = nullptr;                // d_argmax + 1
     unsigned long long* d_trace = nullptr;   // phase trace of the persistent step (QDEC_OPT_TRACE)
     int prefill_gemm = QDEC_PREFILL_TCGEN05;
+    int attn_unit_keys = 0;      // QDEC_OPT_ATTN_UNIT_KEYS (0 = default)
     BatchWork* batch = nullptr;          // lockstep-batch workspace when this context led a batch
     int sms = 0;
 
@@ -514,7 +515,7 @@ int enqueue_decode_step(qdec_ctx* c, int token) {
         p.pos = c->position;
         p.token = token;
         p.epoch = ++c->epoch;
-        decode_persistent_chunks(c->dp, c->position + 1, &p.n_chunks, &p.chunk);
+        decode_persistent_chunks(c->dp, c->position + 1, c->attn_unit_keys, &p.n_chunks, &p.chunk);
         p.argmax = c->d_argmax;
         p.pos_out = c->d_pos;
         p.history = c->d_hist;
@@ -923,6 +924,7 @@ int qdec_clone(const qdec_ctx* src, qdec_ctx** out) {
     c->prefilled = src->prefilled;
     if (c->persistent_ok) c->decode_kernel = src->decode_kernel;
     c->prefill_gemm = src->prefill_gemm;
+    c->attn_unit_keys = src->attn_unit_keys;
     *out = c;
     return QDEC_OK;
 }
@@ -968,6 +970,12 @@ int qdec_set_option(qdec_ctx* c, int32_t option, int32_t value) {
         c->prefill_gemm = value;
         return QDEC_OK;
     }
+    if (option == QDEC_OPT_ATTN_UNIT_KEYS) {
+        if (value != 0 && (value < 8 || value > 4096 || value % 8 != 0))
+            return fail(QDEC_E_INVALID_ARG, "QDEC_OPT_ATTN_UNIT_KEYS takes 0 or 8..4096 in multiples of 8");
+        c->attn_unit_keys = value;
+        return QDEC_OK;
+    }
     if (option == QDEC_OPT_TRACE) {
         if (value != 0 && value != 1) return fail(QDEC_E_INVALID_ARG, "QDEC_OPT_TRACE takes 0 or 1");
         if (value == 1 && !c->persistent_ok) return fail(QDEC_E_UNSUPPORTED, "no persistent decode kernel to trace");
@@ -995,6 +1003,7 @@ int qdec_get_option(const qdec_ctx* c, int32_t option) {
     if (!c) return fail(QDEC_E_INVALID_ARG, "null context");
     if (option == QDEC_OPT_TRACE) return c->d_trace ? 1 : 0;
     if (option == QDEC_OPT_PREFILL_IMPL) return c->prefill_gemm;
+    if (option == QDEC_OPT_ATTN_UNIT_KEYS) return c->attn_unit_keys;
     if (option != QDEC_OPT_DECODE_KERNEL) return fail(QDEC_E_INVALID_ARG, "unknown option %d", option);
     return c->decode_kernel;
 }

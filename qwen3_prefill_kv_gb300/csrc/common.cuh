@@ -209,7 +209,8 @@ struct DecodeLaunch {
 // Chooses the instantiation, ring depth and grid for `sh` on `device`; cudaErrorNotSupported
 // when the persistent kernel does not cover the shape or the device.
 cudaError_t decode_persistent_plan(const Shape& sh, int device, DecodeLaunch* out);
-void decode_persistent_chunks(const DecodeLaunch& cfg, int L, int* n_chunks, int* chunk);
+// keys: positions per attention unit (0 = 256).
+void decode_persistent_chunks(const DecodeLaunch& cfg, int L, int keys, int* n_chunks, int* chunk);
 cudaError_t launch_decode_persistent(const DecodeParams& p, const DecodeLaunch& cfg, cudaStream_t s);
 
 }  // namespace qdec

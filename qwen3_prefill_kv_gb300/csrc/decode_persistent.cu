@@ -1179,13 +1179,21 @@ cudaError_t decode_persistent_plan(const Shape& sh, int device, DecodeLaunch* ou
     return cudaSuccess;
 }
 
-void decode_persistent_chunks(const DecodeLaunch& cfg, int L, int* n_chunks, int* chunk) {
-    // about 256 keys per attention unit, at most one unit per CTA
-    int n = (L + 255) / 256;
+void decode_persistent_chunks(const DecodeLaunch& cfg, int L, int keys, int* n_chunks, int* chunk) {
+    // about `keys` keys per attention unit, at most one unit per CTA.  Default (keys = 0):
+    // one unit up to 160 keys (a split costs a merge of ~1 us per layer), else ~64 keys per
+    // unit (measured on GB300 at KV length 416-543: 256 keys 0.754, 128 keys 0.705, 64 keys
+    // 0.684, 32 keys 0.735 ms/token; at length <= 128 one unit beats two by 4%)
+    // The default rounds a split unit up to whole 64-position ring stages (at KV length ~4100,
+    // 17 units of 256 keys measured 4% faster than 19 units of 232).
+    int n;
+    if (keys > 0) n = (L + keys - 1) / keys;
+    else n = L <= 160 ? 1 : (L + 63) / 64;
     if (n > cfg.max_chunks) n = cfg.max_chunks;
     if (n < 1) n = 1;
     int ch = (L + n - 1) / n;
-    ch = (ch + 7) / 8 * 8;
+    const int align = (keys == 0 && n > 1) ? 64 : 8;
+    ch = (ch + align - 1) / align * align;
     n = (L + ch - 1) / ch;
     *n_chunks = n;
     *chunk = ch;

@@ -276,3 +276,39 @@ def test_errors_leave_context_unchanged(model):
         dec.decode_step(6)                           # slot 33 >= max_seq
     assert e.value.status == -2
     assert dec.position == 33
+
+
+@pytest.mark.parametrize("keys", [8, 24, 4096])
+def test_attention_unit_size_option(model, keys):
+    """QDEC_OPT_ATTN_UNIT_KEYS only changes how the persistent step splits the KV history
+    into attention units (and so the summation order): logits agree with the default split
+    to fp32 rounding, teacher-forced parity against the oracle holds, and clones inherit it."""
+    w, wd, orc = model
+    p = _prompt(12, 50, 15)
+    a = Decoder(SH, wd, max_seq=p.ids.numel() + 6)
+    b = Decoder(SH, wd, max_seq=p.ids.numel() + 6)
+    b.set_option(_lib.OPT_ATTN_UNIT_KEYS, keys)
+    assert b.get_option(_lib.OPT_ATTN_UNIT_KEYS) == keys
+    la = torch.empty(SH.vocab, device="cuda"); lb = torch.empty(SH.vocab, device="cuda")
+    a.prefill(p.ids, p.audio.cuda(), p.audio_offset)
+    b.prefill(p.ids, p.audio.cuda(), p.audio_offset)
+    c = b.clone()
+    assert c.get_option(_lib.OPT_ATTN_UNIT_KEYS) == keys
+    for t in (5, 9, 13, 2):
+        ta = a.decode_step(t, logits=la)
+        tb = b.decode_step(t, logits=lb)
+        ga, gb = la.cpu().double().numpy(), lb.cpu().double().numpy()
+        assert np.abs(ga - gb).max() <= 1e-4 * np.abs(ga).max()
+        assert tb == int(np.argmax(gb))
+    d = Decoder(SH, wd, max_seq=p.ids.numel() + 6)
+    d.set_option(_lib.OPT_ATTN_UNIT_KEYS, keys)
+    H.assert_step_parity(H.teacher_forced(d, orc, p, 5), f"tiny unit keys {keys}")
+
+
+def test_attention_unit_size_option_rejects_bad_values(model):
+    w, wd, orc = model
+    d = Decoder(SH, wd, max_seq=40)
+    for v in (-8, 4, 12, 4104):
+        with pytest.raises(QdecError):
+            d.set_option(_lib.OPT_ATTN_UNIT_KEYS, v)
+    assert d.get_option(_lib.OPT_ATTN_UNIT_KEYS) == 0
