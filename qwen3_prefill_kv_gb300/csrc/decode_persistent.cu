@@ -1078,28 +1078,46 @@ __global__ void __launch_bounds__(NT, 1) decode_persistent_kernel(const DecodePa
             bi[warp] = besti;
         }
         consumer_sync();
-        if (threadIdx.x == 0) {
-            float b = bv[0];
-            int ib = bi[0];
-            for (int w = 1; w < NCW; ++w)
-                if (am_better(bv[w], bi[w], b, ib)) { b = bv[w]; ib = bi[w]; }
-            p.am_part[c].v = b;
-            p.am_part[c].i = ib;
-            __threadfence();
-            const unsigned int tk = atomicAdd(p.am_count, 1u);
+        if (warp == 0) {
+            // lane 0 publishes this CTA's best and takes a ticket; the last CTA's warp 0 reads
+            // the grid's partials 32 at a time (the loads overlap) and reduces them
+            unsigned int tk = 0;
+            if (lane == 0) {
+                float b = bv[0];
+                int ib = bi[0];
+                for (int w = 1; w < NCW; ++w)
+                    if (am_better(bv[w], bi[w], b, ib)) { b = bv[w]; ib = bi[w]; }
+                p.am_part[c].v = b;
+                p.am_part[c].i = ib;
+                __threadfence();
+                tk = atomicAdd(p.am_count, 1u);
+            }
+            tk = __shfl_sync(0xffffffffu, tk, 0);
             if (tk == (unsigned int)nc - 1) {
                 __threadfence();
-                for (int j = 0; j < nc; ++j) {
+                float b = -INFINITY;
+                int ib = 0x7fffffff;
+                for (int j = lane; j < nc; j += 32) {
                     const float v = __ldcg(&p.am_part[j].v);
                     const int i = __ldcg(&p.am_part[j].i);
                     if (am_better(v, i, b, ib)) { b = v; ib = i; }
                 }
-                if (volatile_load(p.err) == 0) {
-                    *p.argmax = (ib == 0x7fffffff) ? 0 : ib;
-                    *p.pos_out = p.pos + 1;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, b, o);
+                    const int oi = __shfl_xor_sync(0xffffffffu, ib, o);
+                    if (am_better(ov, oi, b, ib)) { b = ov; ib = oi; }
                 }
-                *p.am_count = 0u;
+                if (lane == 0) {
+                    if (volatile_load(p.err) == 0) {
+                        *p.argmax = (ib == 0x7fffffff) ? 0 : ib;
+                        *p.pos_out = p.pos + 1;
+                    }
+                    *p.am_count = 0u;
+                }
             }
+        }
+        if (threadIdx.x == 0) {
             trace_mark(p, 10 * p.NL + 3);
             if (p.trace) {
                 p.trace[(size_t)blockIdx.x * (11 * p.NL + 8) + 11 * p.NL + 5] = reinterpret_cast<unsigned long long*>(S.flags + 4)[0];
