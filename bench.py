@@ -72,7 +72,7 @@ def workload_desc(wl):
 # kernel, from the ncu capture summarised in profiles/decode_persistent_funasr_nano_short.md
 # (11th decode step of funasr_nano_short).  Reported only for that workload; it must be
 # re-captured (or dropped) whenever the kernel changes.
-PROFILED_DECODE_TRAFFIC = {"funasr_nano_short": 1_204_232_704}
+PROFILED_DECODE_TRAFFIC = {"funasr_nano_short": 1_204_322_048}
 
 
 def decode_step_bytes(shape, L):
