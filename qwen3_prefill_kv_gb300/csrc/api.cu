@@ -158,6 +158,20 @@ struct qdec_ctx {
 
     cudaGraphExec_t decode_exec = nullptr;
     uint64_t decode_graph_kernels = 0;   // kernel nodes in decode_exec
+    // Prefill bodies (layers, head, position) as CUDA graphs, one per (prompt length,
+    // implementation, GEMM tile width); a length is captured on its second prefill.
+    struct PrefillGraph {
+        int T, impl, tile;
+        int uses;                        // eager prefills of this key before capture
+        cudaGraphExec_t exec;
+        uint64_t kernels;
+    };
+    std::vector<PrefillGraph> pf_graphs;
+    void drop_prefill_graphs() {
+        for (auto& g : pf_graphs)
+            if (g.exec) cudaGraphExecDestroy(g.exec);
+        pf_graphs.clear();
+    }
 
     // persistent single-kernel decode step
     int decode_kernel = QDEC_DECODE_PERSISTENT;
@@ -196,6 +210,7 @@ void free_all(qdec_ctx* c) {
         c->batch = nullptr;
     }
     if (c->decode_exec) cudaGraphExecDestroy(c->decode_exec);
+    c->drop_prefill_graphs();
     void* ptrs[] = {c->kv, c->rope, c->d_hist, c->d_pos, c->d_zero, c->d_argmax, c->d_x, c->d_qkv, c->d_q,
                     c->d_attn, c->d_h, c->d_logits, c->d_part_ml, c->d_part_o, c->d_lm_scratch, c->p_X,
                     c->p_qkv, c->p_Xn, c->p_Q, c->p_O, c->p_H, c->p_ids, c->p_audio, c->p_part, c->d_layers, c->ll_x,
@@ -324,6 +339,7 @@ int ensure_prefill_scratch(qdec_ctx* c, int T) {
         c->part_cap = cap;
     }
     if (T <= c->pf_cap) return QDEC_OK;
+    c->drop_prefill_graphs();   // they hold the buffers about to be replaced
     const Shape& sh = c->sh;
     void* old[] = {c->p_X, c->p_qkv, c->p_Xn, c->p_Q, c->p_O, c->p_H, c->p_ids};
     CK(cudaStreamSynchronize(c->stream));
@@ -386,10 +402,9 @@ int prefill_splits(const qdec_ctx* c, int M, int N, int K, int lda) {
 // One layer of the prefill over T rows starting at position 0.  *fold carries split-K
 // partials of the previous down projection still to be added into the residual (0 = none);
 // *kernels counts the launches.
-int prefill_layer(qdec_ctx* c, int l, int T, int* fold, uint64_t* kernels) {
+int prefill_layer(qdec_ctx* c, int l, int T, int* fold, uint64_t* kernels, cudaStream_t s) {
     const Shape& sh = c->sh;
     const LayerW& w = c->layers[l];
-    cudaStream_t s = c->stream;
     const int qd = sh.HQ * sh.D, nq = sh.qkv_rows();
     uint64_t k = 0;
     if (*fold > 1)
@@ -800,6 +815,81 @@ int qdec_create(const qdec_config* cfg, const qdec_weights* w, void* cuda_stream
     return QDEC_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// The prefill after the embedding: the layers, the fold of the last split-K partials, the
+// tied head on the last row and the device position, queued on s.
+int prefill_body(qdec_ctx* c, int T, cudaStream_t s, uint64_t* kernels) {
+    const Shape& sh = c->sh;
+    uint64_t k = 2;   // lm_head, position
+    int fold = 0;
+    for (int l = 0; l < sh.NL; ++l) {
+        const int rc = prefill_layer(c, l, T, &fold, &k, s);
+        if (rc != QDEC_OK) return rc;
+    }
+    if (fold > 1) {   // the last down projection's partials, for the row the head reads
+        const size_t last = (size_t)(T - 1) * sh.H;
+        CK(launch_fold_partials(c->p_X + last, c->p_part + last, fold, (size_t)T * sh.H, (size_t)sh.H, s));
+        ++k;
+    }
+    CK(launch_lm_head_argmax(c->embed, sh.V, sh.H, c->p_X + (size_t)(T - 1) * sh.H, c->final_norm, sh.eps,
+                             c->d_logits, c->d_argmax, c->d_lm_scratch, s));
+    CK(launch_set_int(c->d_pos, T, s));
+    *kernels += k;
+    return QDEC_OK;
+}
+
+// Runs the prefill body on the context's stream: eagerly the first time a (length,
+// implementation, tile width) key is seen, from a CUDA graph captured on the second and
+// replayed after that (about 250 launches for a short prompt become one).
+int prefill_run_body(qdec_ctx* c, int T, uint64_t* kernels) {
+    const int tile = set_gemm_tile_width(0);
+    set_gemm_tile_width(tile);   // read the process-wide setting back unchanged
+    qdec_ctx::PrefillGraph* g = nullptr;
+    for (auto& e : c->pf_graphs)
+        if (e.T == T && e.impl == c->prefill_gemm && e.tile == tile) g = &e;
+    if (g && g->exec) {
+        CK(cudaGraphLaunch(g->exec, c->stream));
+        *kernels += g->kernels;
+        return QDEC_OK;
+    }
+    if (!g) {
+        if (c->pf_graphs.size() >= 8) {   // keep a few keys; forget the oldest
+            if (c->pf_graphs.front().exec) cudaGraphExecDestroy(c->pf_graphs.front().exec);
+            c->pf_graphs.erase(c->pf_graphs.begin());
+        }
+        c->pf_graphs.push_back(qdec_ctx::PrefillGraph{T, c->prefill_gemm, tile, 0, nullptr, 0});
+        g = &c->pf_graphs.back();
+    }
+    if (g->uses++ == 0) return prefill_body(c, T, c->stream, kernels);   // first use: eager
+    cudaGraph_t graph = nullptr;
+    uint64_t k = 0;
+    CK(cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal));
+    int rc = prefill_body(c, T, c->cap_stream, &k);
+    cudaError_t e = cudaStreamEndCapture(c->cap_stream, &graph);
+    if (rc != QDEC_OK) {
+        if (graph) cudaGraphDestroy(graph);
+        return rc;
+    }
+    if (e == cudaSuccess) e = cudaGraphInstantiate(&g->exec, graph, 0);
+    if (graph) cudaGraphDestroy(graph);
+    if (e != cudaSuccess) {
+        g->exec = nullptr;
+        cudaGetLastError();
+        return prefill_body(c, T, c->stream, kernels);   // could not capture: run eagerly
+    }
+    g->kernels = k;
+    CK(cudaGraphLaunch(g->exec, c->stream));
+    *kernels += k;
+    return QDEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 int qdec_prefill(qdec_ctx* c, const int32_t* ids, int32_t n_ids, const void* audio_rows, int32_t n_audio,
                  int32_t audio_offset, float* logits_out, int32_t* argmax_out) {
     if (!c || !ids) return fail(QDEC_E_INVALID_ARG, "null context or ids");
@@ -831,20 +921,9 @@ int qdec_prefill(qdec_ctx* c, const int32_t* ids, int32_t n_ids, const void* aud
     c->prefilled = false;
     c->position = 0;
     CK(launch_embed_splice(c->embed, c->p_ids, T, sh.H, audio, n_audio, audio_offset, c->p_X, c->d_hist, s));
-    uint64_t kernels = 3;   // embed, lm_head, position
-    int fold = 0;
-    for (int l = 0; l < sh.NL; ++l) {
-        rc = prefill_layer(c, l, T, &fold, &kernels);
-        if (rc != QDEC_OK) return rc;
-    }
-    if (fold > 1) {   // the last down projection's partials, for the row the head reads
-        const size_t last = (size_t)(T - 1) * sh.H;
-        CK(launch_fold_partials(c->p_X + last, c->p_part + last, fold, (size_t)T * sh.H, (size_t)sh.H, s));
-        ++kernels;
-    }
-    CK(launch_lm_head_argmax(c->embed, sh.V, sh.H, c->p_X + (size_t)(T - 1) * sh.H, c->final_norm, sh.eps,
-                             c->d_logits, c->d_argmax, c->d_lm_scratch, s));
-    CK(launch_set_int(c->d_pos, T, s));
+    uint64_t kernels = 1;
+    rc = prefill_run_body(c, T, &kernels);
+    if (rc != QDEC_OK) return rc;
     count_launches(kernels);
     c->position = T;
     c->prefilled = true;

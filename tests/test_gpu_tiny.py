@@ -312,3 +312,30 @@ def test_attention_unit_size_option_rejects_bad_values(model):
         with pytest.raises(QdecError):
             d.set_option(_lib.OPT_ATTN_UNIT_KEYS, v)
     assert d.get_option(_lib.OPT_ATTN_UNIT_KEYS) == 0
+
+
+def test_repeated_prefill_replays_identically(model):
+    """The second prefill of a prompt length is captured as a CUDA graph and later ones
+    replay it: logits, argmax and the decode steps that follow are bitwise those of the
+    first (eager) prefill, also when other lengths are prefilled in between."""
+    w, wd, orc = model
+    p = _prompt(12, 50, 15)
+    q = _prompt(3, 20, 4, seed=1)
+    dec = Decoder(SH, wd, max_seq=p.ids.numel() + 4)
+    lg = torch.empty(SH.vocab, device="cuda")
+    runs = []
+    for i in range(4):
+        if i == 2:
+            dec.prefill(q.ids, q.audio.cuda(), q.audio_offset)   # another length in between
+        a = dec.prefill(p.ids, p.audio.cuda(), p.audio_offset, logits=lg)
+        seq = [lg.clone()]
+        toks = [a]
+        for t in (3, -1, -1):
+            toks.append(dec.decode_step(t, logits=lg))
+            seq.append(lg.clone())
+        runs.append((toks, torch.stack(seq)))
+        assert dec.position == p.ids.numel() + 3
+    for toks, seq in runs[1:]:
+        assert toks == runs[0][0]
+        assert torch.equal(seq, runs[0][1])
+    H.assert_step_parity(H.teacher_forced(dec, orc, p, 3), "tiny prefill replay")
