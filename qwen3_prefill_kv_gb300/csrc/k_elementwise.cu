@@ -102,10 +102,36 @@ __global__ void rmsnorm_bf16_kernel(const float* __restrict__ X, int H, const bf
     }
 }
 
+// H = 1024 (the 0.6B shape): 128 threads per row, each holding 8 values in registers (two
+// 16-byte loads in flight), so a row is read once and twice as many rows are in flight per
+// SM as with 256 threads.
+__global__ void __launch_bounds__(128) rmsnorm1024_bf16_kernel(const float* __restrict__ X,
+                                                               const bf16_t* __restrict__ g, float eps,
+                                                               bf16_t* __restrict__ out) {
+    __shared__ float red[4];
+    const float4* x = reinterpret_cast<const float4*>(X + (size_t)blockIdx.x * 1024);
+    const int t = threadIdx.x;
+    const float4 a = x[t], b = x[t + 128];
+    float ss = a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w;
+    ss = warp_sum(ss);
+    if ((t & 31) == 0) red[t >> 5] = ss;
+    __syncthreads();
+    const float r = rsqrtf((red[0] + red[1] + red[2] + red[3]) / 1024.f + eps);
+    const uint2 ga = reinterpret_cast<const uint2*>(g)[t], gb = reinterpret_cast<const uint2*>(g)[t + 128];
+    uint2* o = reinterpret_cast<uint2*>(out + (size_t)blockIdx.x * 1024);
+    o[t] = make_uint2(pack_bf2(a.x * r * bf_lo(ga.x), a.y * r * bf_hi(ga.x)),
+                      pack_bf2(a.z * r * bf_lo(ga.y), a.w * r * bf_hi(ga.y)));
+    o[t + 128] = make_uint2(pack_bf2(b.x * r * bf_lo(gb.x), b.y * r * bf_hi(gb.x)),
+                            pack_bf2(b.z * r * bf_lo(gb.y), b.w * r * bf_hi(gb.y)));
+}
+
 cudaError_t launch_rmsnorm_bf16(const float* X, int T, int H, const bf16_t* g, float eps, bf16_t* out,
                                 cudaStream_t s) {
     (void)cudaGetLastError();   // attribute only this launch's errors
-    rmsnorm_bf16_kernel<<<T, 256, 0, s>>>(X, H, g, eps, out);
+    if (H == 1024)
+        rmsnorm1024_bf16_kernel<<<T, 128, 0, s>>>(X, g, eps, out);
+    else
+        rmsnorm_bf16_kernel<<<T, 256, 0, s>>>(X, H, g, eps, out);
     return cudaGetLastError();
 }
 
