@@ -7,7 +7,7 @@ import torch
 import oracle
 from qwen3_prefill_kv_gb300 import synth
 
-# BASELINE tolerance for teacher-forced logits: cosine >= 0.9995 and
+# The parity gate for teacher-forced logits: cosine >= 0.9995 and
 # max|d| <= 1e-2 * max|oracle logit|, argmax equal wherever the oracle's
 # top-1/top-2 gap exceeds that bound.
 COS_MIN = 0.9995
