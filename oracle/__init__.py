@@ -8,6 +8,9 @@ hand it plain arrays (the seeded inputs) and compare its results with the GPU's.
 
 Every function computes in float64 (see ``decoder.py`` for the reading of the
 pages this follows).  Parity is pinned by ``tests/test_oracle_pins.py``.
+``sampling.py`` is the token choice after the lm_head (greedy, temperature, top-k,
+top-p, repetition penalty, counter-based draws), pinned by
+``tests/test_oracle_sampling.py``.
 """
 from .decoder import (DecoderOracle, rms_norm, rope_inv_freq, rope_neox, causal_gqa_attention,
                       swiglu, inputs_embeds, tied_lm_head, greedy_argmax, fake_token_len)
