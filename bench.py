@@ -53,6 +53,24 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def reduce_max_over_ranks(values, world, device):
+    """Element-wise maximum of `values` over the ranks (identity for one process): the
+    slowest replica's times define the whole job's."""
+    if world == 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(world, units_per_rank, seconds):
+    """Units per second of the whole job: each of `world` replicas processed
+    `units_per_rank` units, the slowest within `seconds`."""
+    return world * units_per_rank / seconds
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -291,20 +309,16 @@ def run_ours(args):
             e_dec.append(time.perf_counter() - t1)
         h2d = ids.numel() * 4 + prompt.audio.numel() * 2 + wl.n_decode * 4
         d2h = (wl.n_decode + 1) * 4 + shape.vocab * 4
-        e2e_val = wl.n_decode * len(e_dec) / sum(e_dec)
-        e2e = {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_token": 1e3 * sum(e_dec) / (wl.n_decode * len(e_dec))}
+        e_total, = reduce_max_over_ranks([sum(e_dec)], world, dev)
+        e2e = {"value": whole_job_rate(world, wl.n_decode * len(e_dec), e_total), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_token": 1e3 * e_total / (wl.n_decode * len(e_dec))}
 
     dec_total_s = sum(dec_ms) / 1e3
     pre_total_s = sum(pre_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([dec_total_s, pre_total_s, sum(tot_ms)], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dec_total_s, pre_total_s, tot = t.tolist()
-        tot_ms_mean = tot / args.steps
-    else:
-        tot_ms_mean = sum(tot_ms) / args.steps
-    value = world * wl.n_decode * args.steps / dec_total_s
+    dec_total_s, pre_total_s, tot = reduce_max_over_ranks([dec_total_s, pre_total_s, sum(tot_ms)], world, dev)
+    tot_ms_mean = tot / args.steps
+    value = whole_job_rate(world, wl.n_decode * args.steps, dec_total_s)
     hbm, bf16, peak_kind = peaks()
     # roofline of the decode step (the dominant part of the step): algorithmic bytes per
     # step averaged over the KV lengths the timed steps see, over the mean step time.
@@ -314,7 +328,7 @@ def run_ours(args):
     achieved = bytes_per_token / t_tok / 1e9
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": tot_ms_mean, "ms_per_token": 1e3 * t_tok,
-            "prefill_tok_s": world * wl.n_prompt * args.steps / pre_total_s,
+            "prefill_tok_s": whole_job_rate(world, wl.n_prompt * args.steps, pre_total_s),
             "prefill_ms": 1e3 * pre_total_s / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded random-init bf16 weights of the Qwen3-0.6B shape; seeded ids and audio rows)",
@@ -418,17 +432,16 @@ def run_ours_batch(args, wl, dec, prompt, audio_dev, stream, dev, rank, world, l
         e_dec = [step_host() for _ in range(args.steps)]
         h2d = prompt.ids.numel() * 4 + prompt.audio.numel() * 2 + wl.n_decode * n * 4
         d2h = (wl.n_decode + 1) * n * 4 + n * shape.vocab * 4
-        e2e = {"value": n * wl.n_decode * len(e_dec) / sum(e_dec), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_lockstep": 1e3 * sum(e_dec) / (wl.n_decode * len(e_dec))}
+        e_total, = reduce_max_over_ranks([sum(e_dec)], world, dev)
+        e2e = {"value": whole_job_rate(world, n * wl.n_decode * len(e_dec), e_total), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_lockstep": 1e3 * e_total / (wl.n_decode * len(e_dec))}
 
     dec_total_s = sum(dec_ms) / 1e3
     pre_total_s = sum(pre_ms) / 1e3
     tot_ms_mean = (sum(dec_ms) + sum(pre_ms)) / args.steps
-    if world > 1:
-        t = torch.tensor([dec_total_s, pre_total_s, tot_ms_mean], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dec_total_s, pre_total_s, tot_ms_mean = t.tolist()
-    value = world * n * wl.n_decode * args.steps / dec_total_s
+    dec_total_s, pre_total_s, tot_ms_mean = reduce_max_over_ranks([dec_total_s, pre_total_s, tot_ms_mean], world, dev)
+    value = whole_job_rate(world, n * wl.n_decode * args.steps, dec_total_s)
     hbm, _, peak_kind = peaks()
     t_lock = dec_total_s / (wl.n_decode * args.steps)
     bytes_per_lock = sum(batch_step_bytes(shape, [wl.n_prompt + 1 + j] * n) for j in range(wl.n_decode)) / wl.n_decode
