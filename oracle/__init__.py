@@ -10,7 +10,8 @@ Every function computes in float64 (see ``decoder.py`` for the reading of the
 pages this follows).  Parity is pinned by ``tests/test_oracle_pins.py``.
 ``sampling.py`` is the token choice after the lm_head (greedy, temperature, top-k,
 top-p, repetition penalty, counter-based draws), pinned by
-``tests/test_oracle_sampling.py``.
+``tests/test_oracle_sampling.py``; ``adaptor.py`` is the projector and bidirectional
+adaptor that produce the audio rows, pinned by ``tests/test_oracle_adaptor.py``.
 """
 from .decoder import (DecoderOracle, rms_norm, rope_inv_freq, rope_neox, causal_gqa_attention,
                       swiglu, inputs_embeds, tied_lm_head, greedy_argmax, fake_token_len)

@@ -229,3 +229,55 @@ def make_tokens(vocab: int, n: int, seed: int = 0, tag: int = 3) -> torch.Tensor
     """``n`` token ids uniform on [0, vocab) (forced first tokens of clones, etc.)."""
     g = torch.Generator().manual_seed(_stream_seed(seed, tag))
     return torch.randint(0, vocab, (n,), generator=g, dtype=torch.int64).to(torch.int32)
+
+
+# ------------------------------------------------------------------ audio adaptor inputs
+@dataclass(frozen=True)
+class AdaptorShape:
+    """The projector and bidirectional adaptor that turn encoder frames into the audio rows
+    spliced into the prompt ("Forward map - funasr_nano", adaptor table: linear1 512 -> 2048
+    + ReLU, linear2 2048 -> 1024, two blocks of LayerNorm + multi-head attention + a
+    1024 -> 256 -> 1024 ReLU FFN; "Fun-ASR-Nano Native Runtime Implementation Plan", Task 5:
+    eight heads)."""
+    enc_dim: int = 512
+    proj_dim: int = 2048
+    hidden: int = 1024
+    n_heads: int = 8
+    ffn: int = 256
+    n_blocks: int = 2
+    ln_eps: float = 1.0e-12
+
+
+ADAPTOR = AdaptorShape()
+ADAPTOR_TINY = AdaptorShape(enc_dim=24, proj_dim=40, hidden=32, n_heads=4, ffn=8, n_blocks=2)
+
+
+def make_adaptor_weights(shape: AdaptorShape, seed: int = 0, weight_std: float = 0.02) -> dict:
+    """Random-init float32 adaptor weights: matrices N(0, weight_std), biases N(0, 0.02),
+    LayerNorm gains 1 + N(0, 0.1) and biases N(0, 0.1) (non-trivial, so a dropped affine
+    term shows), drawn from one Generator seeded with _stream_seed(seed, 16) in the order
+    listed; matrices row-major [out, in]."""
+    g = torch.Generator().manual_seed(_stream_seed(seed, 16))
+
+    def mat(o, i):
+        return torch.randn(o, i, generator=g) * weight_std
+
+    def vec(n, std, mean=0.0):
+        return torch.randn(n, generator=g) * std + mean
+
+    E, P, H, F = shape.enc_dim, shape.proj_dim, shape.hidden, shape.ffn
+    w = {"w1": mat(P, E), "b1": vec(P, 0.02), "w2": mat(H, P), "b2": vec(H, 0.02), "blocks": []}
+    for _ in range(shape.n_blocks):
+        w["blocks"].append({
+            "ln1_g": vec(H, 0.1, 1.0), "ln1_b": vec(H, 0.1),
+            "wq": mat(H, H), "bq": vec(H, 0.02), "wk": mat(H, H), "bk": vec(H, 0.02),
+            "wv": mat(H, H), "bv": vec(H, 0.02), "wo": mat(H, H), "bo": vec(H, 0.02),
+            "ln2_g": vec(H, 0.1, 1.0), "ln2_b": vec(H, 0.1),
+            "fc1": mat(F, H), "fc1_b": vec(F, 0.02), "fc2": mat(H, F), "fc2_b": vec(H, 0.02)})
+    return w
+
+
+def make_encoder_frames(shape: AdaptorShape, n_frames: int, seed: int = 0) -> torch.Tensor:
+    """Encoder output frames [n_frames, enc_dim], N(0, 1) float32."""
+    g = torch.Generator().manual_seed(_stream_seed(seed, 17))
+    return torch.randn(n_frames, shape.enc_dim, generator=g)
