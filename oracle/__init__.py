@@ -11,7 +11,9 @@ pages this follows).  Parity is pinned by ``tests/test_oracle_pins.py``.
 ``sampling.py`` is the token choice after the lm_head (greedy, temperature, top-k,
 top-p, repetition penalty, counter-based draws), pinned by
 ``tests/test_oracle_sampling.py``; ``adaptor.py`` is the projector and bidirectional
-adaptor that produce the audio rows, pinned by ``tests/test_oracle_adaptor.py``.
+adaptor that produce the audio rows, pinned by ``tests/test_oracle_adaptor.py``;
+``quant.py`` is the library's block-quantized weight formats, pinned by
+``tests/test_oracle_quant.py``.
 """
 from .decoder import (DecoderOracle, rms_norm, rope_inv_freq, rope_neox, causal_gqa_attention,
                       swiglu, inputs_embeds, tied_lm_head, greedy_argmax, fake_token_len)
