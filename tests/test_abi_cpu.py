@@ -88,3 +88,13 @@ def test_op_entry_points_validate_on_host(lib):
     assert lib.qdec_op_attention_prefill(None, 1, 4, 2, 32, 8, 0, None, None, None, 0, None) == -1
     assert lib.qdec_op_lm_head_scratch_bytes(1024) > 16
     assert lib.qdec_op_lm_head_argmax(None, 1024, 128, None, None, 1e-6, None, None, None, 0, None) == -1
+
+
+def test_gemm_tile_width_setting_without_a_gpu(lib):
+    """qdec_op_gemm_tile_width only sets the process-wide choice: 0, 128 and 256 are taken
+    and the previous value returned; anything else is INVALID_ARG and changes nothing."""
+    assert lib.qdec_op_gemm_tile_width(256) == 0
+    assert lib.qdec_op_gemm_tile_width(128) == 256
+    assert lib.qdec_op_gemm_tile_width(192) == -1
+    assert lib.qdec_op_gemm_tile_width(0) == 128
+    assert lib.qdec_op_gemm_tile_width(0) == 0
