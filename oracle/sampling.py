@@ -90,9 +90,14 @@ def top_p_mask(z, keep, p: float) -> np.ndarray:
     m = z[keep].max()
     w = np.where(keep, np.exp(z - m), 0.0)
     prob = w / w.sum()
+    idx = np.flatnonzero(keep)
+    s = prob[idx]
+    order = np.argsort(-s, kind="stable")
+    sd = s[order]                                   # descending
+    csum = np.concatenate(([0.0], np.cumsum(sd)))   # csum[j] = mass of sd[:j]
+    first = np.searchsorted(-sd, -sd, side="left")  # first index of each value's tie group
     out = np.zeros_like(keep)
-    for i in np.flatnonzero(keep):
-        out[i] = prob[keep & (prob > prob[i])].sum() < p
+    out[idx[order]] = csum[first] < p               # mass strictly more probable < p
     return out
 
 
