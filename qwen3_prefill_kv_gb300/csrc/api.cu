@@ -850,8 +850,7 @@ int prefill_body(qdec_ctx* c, int T, cudaStream_t s, uint64_t* kernels) {
 // implementation, tile width) key is seen, from a CUDA graph captured on the second and
 // replayed after that (about 250 launches for a short prompt become one).
 int prefill_run_body(qdec_ctx* c, int T, uint64_t* kernels) {
-    const int tile = set_gemm_tile_width(0);
-    set_gemm_tile_width(tile);   // read the process-wide setting back unchanged
+    const int tile = gemm_tile_width();
     qdec_ctx::PrefillGraph* g = nullptr;
     for (auto& e : c->pf_graphs)
         if (e.T == T && e.impl == c->prefill_gemm && e.tile == tile) g = &e;

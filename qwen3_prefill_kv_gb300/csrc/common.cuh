@@ -98,6 +98,7 @@ int gemm_tc_splits(int K, int splits);
 // Forces the tcgen05 GEMM's tile width (128 or 256; 0 = chosen per shape); returns the previous
 // setting.  Process-wide, not thread-safe: for tuning and tests.
 int set_gemm_tile_width(int bn);
+int gemm_tile_width();   // the current setting (0, 128 or 256)
 cudaError_t launch_gemm_tc(const bf16_t* A, int lda, const bf16_t* W, int M, int N, int K, int mode, int up_off,
                            float* Cf, bf16_t* Cb, int ldc, cudaStream_t s, int splits = 1);
 // The packed QKV projection with the per-head epilogue fused (head_dim 128, one head per

@@ -470,6 +470,8 @@ int set_gemm_tile_width(int bn) {
     return prev;
 }
 
+int gemm_tile_width() { return g_tile_width; }
+
 bool gemm_tc_supported(int N, int K, int mode, int lda) {
     if (K % BK != 0 || lda % 8 != 0) return false;
     if (mode == GEMM_SWIGLU_BF16) return N % 64 == 0;
