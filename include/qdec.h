@@ -171,6 +171,30 @@ int qdec_set_option(qdec_ctx *ctx, int32_t option, int32_t value);
 /* Current value of an option, or a negative code. */
 int qdec_get_option(const qdec_ctx *ctx, int32_t option);
 
+/* Token choice of qdec_prefill and qdec_decode_step ("Qwen3ASR ncnn多平台移植" §1: greedy,
+ * temperature, top-k, top-p and repetition penalty; §6: greedy by default).  The page
+ * names the options without defining them; this library applies, in order:
+ *   1. repetition_penalty r over the distinct ids of the context's history (prompt ids
+ *      and the tokens fed so far, the current one included): a positive logit is divided
+ *      by r, a non-positive one multiplied by r (r = 1: no penalty);
+ *   2. temperature T (T = 0: the lowest-index argmax of the penalised logits);
+ *   3. top_k (0: off): keep the logits >= the k-th largest, ties kept;
+ *   4. top_p (1: off): keep a token while the probability of the kept tokens strictly
+ *      more probable than it sums to < top_p, ties kept;
+ *   5. the draw: u = top 24 bits of output pos + 1 of splitmix64 started at state `seed`,
+ *      pos = the position of the logits row (the last prompt position after a prefill,
+ *      the fed token's position after a step); the token is the smallest kept id whose
+ *      cumulative kept probability in id order exceeds u times the kept total.
+ * The choice is deterministic for given logits, history and (seed, pos).  It replaces the
+ * argmax: argmax_out returns it and token = -1 feeds it to the next step.  The returned
+ * logits stay the raw lm_head logits.  Defaults (greedy): T = 0, top_k = 0, top_p = 1,
+ * r = 1.  Clones inherit the setting; qdec_decode_step_batch with n > 1 returns
+ * QDEC_E_UNSUPPORTED for a sampling context (the lockstep batch is greedy).  Errors:
+ * INVALID_ARG for T < 0, top_k < 0, top_p outside (0, 1], r <= 0 or a vocabulary over
+ * 262,144. */
+int qdec_set_sampling(qdec_ctx *ctx, float temperature, int32_t top_k, float top_p, float repetition_penalty,
+                      uint64_t seed);
+
 /* Phase trace of the last persistent decode step (QDEC_OPT_TRACE = 1): one
  * row of 11 * n_layers + 8 entries per CTA of the grid (globaltimer ns).
  * Row layout: [10 l + 2 ph] input ready and [10 l + 2 ph + 1] phase done for

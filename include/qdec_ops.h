@@ -48,6 +48,15 @@ int qdec_op_gemm_splitk(const void *A, int32_t lda, const void *W, int32_t M, in
  * setting, or QDEC_E_INVALID_ARG for any other value. */
 int qdec_op_gemm_tile_width(int32_t bn);
 
+/* The token choice of qdec_set_sampling (include/qdec.h) on one logits vector: logits
+ * fp32 [V] (device), history int32 [n_history] (device ids; ids outside [0, V) are
+ * ignored), the draw at position `pos` under `seed`; *token (device int32) receives the
+ * chosen id.  V <= 262,144.  Errors: INVALID_ARG for null pointers, negative sizes or
+ * parameters outside the ranges of qdec_set_sampling. */
+int qdec_op_sample(const float *logits, int32_t V, const int32_t *history, int32_t n_history, float temperature,
+                   int32_t top_k, float top_p, float repetition_penalty, uint64_t seed, int32_t pos, int32_t *token,
+                   void *stream);
+
 /* Synchronises the device and reports whether a tensor-core kernel launched
  * through these entry points gave up on a bounded wait since the last call:
  * QDEC_OK, or QDEC_E_TIMEOUT (the flag is then cleared). */

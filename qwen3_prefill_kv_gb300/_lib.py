@@ -74,6 +74,8 @@ SIGNATURES = [
     ("qdec_op_gemm", C.c_int, [_VP, _I32, _VP, _I32, _I32, _I32, _I32, _I32, _VP, _I32, _I32, _VP]),
     ("qdec_op_device_error", C.c_int, []),
     ("qdec_op_gemm_tile_width", C.c_int, [C.c_int32]),
+    ("qdec_op_sample", C.c_int, [_VP, _I32, _VP, _I32, _F, _I32, _F, _F, C.c_uint64, _I32, _VP, _VP]),
+    ("qdec_set_sampling", C.c_int, [_VP, _F, _I32, _F, _F, C.c_uint64]),
     ("qdec_op_gemm_splitk", C.c_int, [_VP, _I32, _VP, _I32, _I32, _I32, _I32, _VP, _I32, _VP]),
     ("qdec_op_attention_prefill", C.c_int, [_VP, _I32, _I32, _I32, _I32, _I32, _I32, _VP, _VP, _VP, _I32, _VP]),
     ("qdec_op_lm_head_scratch_bytes", _SZ, [_I32]),
@@ -210,6 +212,12 @@ class Decoder:
     def set_option(self, option: int, value: int) -> None:
         _check(self.lib.qdec_set_option(self.handle, int(option), int(value)))
 
+    def set_sampling(self, temperature: float = 0.0, top_k: int = 0, top_p: float = 1.0,
+                     repetition_penalty: float = 1.0, seed: int = 0) -> None:
+        """Token choice of prefill and decode steps (qdec_set_sampling); defaults are greedy."""
+        _check(self.lib.qdec_set_sampling(self.handle, float(temperature), int(top_k), float(top_p),
+                                          float(repetition_penalty), int(seed) & ((1 << 64) - 1)))
+
     def get_option(self, option: int) -> int:
         r = self.lib.qdec_get_option(self.handle, int(option))
         if r < 0:
@@ -266,6 +274,15 @@ def gemm_tile_width(bn: int) -> int:
     rc = int(load().qdec_op_gemm_tile_width(int(bn)))
     _check(min(rc, 0))
     return rc
+
+
+def sample(logits, V, history, temperature, top_k, top_p, repetition_penalty, seed, pos, token_out,
+           stream=None) -> None:
+    """qdec_op_sample: the token choice on one logits vector into token_out (device int32)."""
+    n = 0 if history is None else int(history.numel())
+    _check(load().qdec_op_sample(_ptr(logits), int(V), _ptr(history) if n else None, n, float(temperature),
+                                 int(top_k), float(top_p), float(repetition_penalty), int(seed) & ((1 << 64) - 1),
+                                 int(pos), _ptr(token_out), _stream_handle(stream)))
 
 
 def device_error() -> None:

@@ -188,6 +188,11 @@ struct qdec_ctx {
     unsigned long long* d_trace = nullptr;   // phase trace of the persistent step (QDEC_OPT_TRACE)
     int prefill_gemm = QDEC_PREFILL_TCGEN05;
     int attn_unit_keys = 0;      // QDEC_OPT_ATTN_UNIT_KEYS (0 = default)
+    // token choice (qdec_set_sampling); greedy while temperature is 0 and penalty 1
+    float samp_t = 0.f, samp_p = 1.f, samp_r = 1.f;
+    int samp_k = 0;
+    unsigned long long samp_seed = 0ull;
+    bool sampling() const { return samp_t != 0.f || samp_r != 1.f; }
     BatchWork* batch = nullptr;          // lockstep-batch workspace when this context led a batch
     int sms = 0;
 
@@ -923,6 +928,11 @@ int qdec_prefill(qdec_ctx* c, const int32_t* ids, int32_t n_ids, const void* aud
     uint64_t kernels = 1;
     rc = prefill_run_body(c, T, &kernels);
     if (rc != QDEC_OK) return rc;
+    if (c->sampling()) {   // the first generated token is drawn at the last prompt position
+        CK(launch_sample(c->d_logits, sh.V, c->d_hist, T, c->samp_t, c->samp_k, c->samp_p, c->samp_r, c->samp_seed,
+                         T - 1, c->d_argmax, s));
+        ++kernels;
+    }
     count_launches(kernels);
     c->position = T;
     c->prefilled = true;
@@ -937,6 +947,11 @@ int qdec_decode_step(qdec_ctx* c, int32_t token, float* logits_out, int32_t* arg
     if (rc != QDEC_OK) return rc;
     rc = enqueue_decode_step(c, token);
     if (rc != QDEC_OK) return rc;
+    if (c->sampling()) {   // replaces the step's argmax; the history holds positions 0 .. position
+        CK(launch_sample(c->d_logits, c->sh.V, c->d_hist, c->position + 1, c->samp_t, c->samp_k, c->samp_p,
+                         c->samp_r, c->samp_seed, c->position, c->d_argmax, c->stream));
+        count_launches(1);
+    }
     c->position += 1;
     rc = copy_logits_out(c, logits_out);
     if (rc != QDEC_OK) return rc;
@@ -955,6 +970,8 @@ int qdec_decode_step_batch(qdec_ctx* const* ctxs, int32_t n, const int32_t* toke
             return fail(QDEC_E_STATE, "batch contexts differ in weights, shape or device");
         for (int j = 0; j < i; ++j)
             if (ctxs[j] == ctxs[i]) return fail(QDEC_E_INVALID_ARG, "context %d repeated in the batch", i);
+        if (n > 1 && ctxs[i]->sampling())
+            return fail(QDEC_E_UNSUPPORTED, "the lockstep batch step is greedy: context %d samples", i);
     }
     if (n == 1) return qdec_decode_step(ctxs[0], tokens[0], logits_out, argmax_out);
     return batch_step(ctxs, n, tokens, logits_out, argmax_out);
@@ -1003,6 +1020,8 @@ int qdec_clone(const qdec_ctx* src, qdec_ctx** out) {
     if (c->persistent_ok) c->decode_kernel = src->decode_kernel;
     c->prefill_gemm = src->prefill_gemm;
     c->attn_unit_keys = src->attn_unit_keys;
+    c->samp_t = src->samp_t; c->samp_p = src->samp_p; c->samp_r = src->samp_r; c->samp_k = src->samp_k;
+    c->samp_seed = src->samp_seed;
     *out = c;
     return QDEC_OK;
 }
@@ -1074,6 +1093,20 @@ int qdec_set_option(qdec_ctx* c, int32_t option, int32_t value) {
     if (value == QDEC_DECODE_PERSISTENT && !c->persistent_ok)
         return fail(QDEC_E_UNSUPPORTED, "the persistent decode kernel does not cover this shape or device");
     c->decode_kernel = value;
+    return QDEC_OK;
+}
+
+int qdec_set_sampling(qdec_ctx* c, float temperature, int32_t top_k, float top_p, float repetition_penalty,
+                      uint64_t seed) {
+    if (!c) return fail(QDEC_E_INVALID_ARG, "null context");
+    if (!sample_params_valid(c->sh.V, temperature, top_k, top_p, repetition_penalty))
+        return fail(QDEC_E_INVALID_ARG, "sampling needs temperature >= 0, top_k >= 0, 0 < top_p <= 1, penalty > 0 "
+                                        "and a vocabulary of at most %d", kSampleMaxVocab);
+    c->samp_t = temperature;
+    c->samp_k = top_k;
+    c->samp_p = top_p;
+    c->samp_r = repetition_penalty;
+    c->samp_seed = (unsigned long long)seed;
     return QDEC_OK;
 }
 

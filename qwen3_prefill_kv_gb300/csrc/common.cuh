@@ -37,6 +37,14 @@ __device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) {
     return v > bv || (v == bv && i < bi);
 }
 
+// Token choice after the lm_head (k_sample.cu): greedy when temperature is 0, else the
+// repetition penalty, temperature, top-k, top-p and a splitmix64 counter draw at `pos`;
+// one CTA, writes *token (device).  The history bitmap limits V to kSampleMaxVocab.
+constexpr int kSampleMaxVocab = 262144;
+bool sample_params_valid(int V, float temperature, int top_k, float top_p, float penalty);
+cudaError_t launch_sample(const float* logits, int V, const int* hist, int n_hist, float temperature, int top_k,
+                          float top_p, float penalty, unsigned long long seed, int pos, int* token, cudaStream_t s);
+
 // Device-side model shape (mirrors qdec_config).
 struct Shape {
     int H, NL, HQ, HKV, D, F, V, max_seq;

@@ -53,6 +53,18 @@ int qdec_op_gemm_tile_width(int32_t bn) {
     return set_gemm_tile_width(bn);
 }
 
+int qdec_op_sample(const float* logits, int32_t V, const int32_t* history, int32_t n_history, float temperature,
+                   int32_t top_k, float top_p, float repetition_penalty, uint64_t seed, int32_t pos, int32_t* token,
+                   void* stream) {
+    if (!logits || !token || n_history < 0 || (n_history > 0 && !history) || pos < 0)
+        return set_error(QDEC_E_INVALID_ARG, "qdec_op_sample: null pointer or negative size/position");
+    if (!sample_params_valid(V, temperature, top_k, top_p, repetition_penalty))
+        return set_error(QDEC_E_INVALID_ARG, "qdec_op_sample: temperature >= 0, top_k >= 0, 0 < top_p <= 1, "
+                                             "penalty > 0, 0 < V <= %d", kSampleMaxVocab);
+    return cuda_status(launch_sample(logits, V, history, n_history, temperature, top_k, top_p, repetition_penalty,
+                                     (unsigned long long)seed, pos, token, static_cast<cudaStream_t>(stream)));
+}
+
 int qdec_op_device_error(void) {
     const int v1 = tc_error_read_and_clear(), v2 = fa_error_read_and_clear();
     if (v1 < 0 || v2 < 0) return set_error(QDEC_E_CUDA, "reading the device error word failed");
