@@ -9,10 +9,13 @@ prompt (20 ids, 23 audio rows, 21 ids) and 64 decode steps.
 
 value  = decode tokens/s (B = 1) over the timed steps, device-timed with CUDA
          events on the decoder's stream, inputs resident in HBM.
-e2e    = the same metric through the C ABI with host buffers: pinned host ids
-         and audio rows copied in every step, every decode step's argmax read
-         back to the host and fed back as the next token, and the last
-         logits vector copied out.
+e2e    = the same metric end to end through the C ABI with host buffers: a
+         whole request is timed (pinned host ids and audio rows copied in, the
+         prefill, every decode step's argmax read back to the host and passed
+         as the next token, the last logits vector copied out); value =
+         generated tokens / request time.
+prefill_roofline = the 4096-position prefill of the long-context workload
+         (the stated tensor-core target), device-timed, against the bf16 peak.
 The weights (1.19 GB) are larger than L2 (129 MB), so no L2 flush is needed
 between steps.
 
@@ -46,6 +49,7 @@ def parse():
     ap.add_argument("--workload", default="funasr_nano_short")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-long-prefill", action="store_true")
     return ap.parse_args()
 
 
@@ -87,10 +91,64 @@ def workload_desc(wl):
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the decode
-# kernel, from the ncu capture summarised in profiles/decode_persistent_funasr_nano_short.md
-# (11th decode step of funasr_nano_short).  Reported only for that workload; it must be
-# re-captured (or dropped) whenever the kernel changes.
-PROFILED_DECODE_TRAFFIC = {"funasr_nano_short": 1_204_322_048}
+# kernel from an ncu capture, with the SHA-256 of the kernel's source files at that capture.
+# The figure is reported only while the sources still hash to that value: any change to the
+# kernel turns it into null until it is captured again.
+PROFILED_DECODE_TRAFFIC = {}
+DECODE_KERNEL_SOURCES = ("qwen3_prefill_kv_gb300/csrc/decode_persistent.cu", "qwen3_prefill_kv_gb300/csrc/common.cuh")
+
+
+def decode_sources_sha():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in DECODE_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_decode_traffic(workload):
+    entry = PROFILED_DECODE_TRAFFIC.get(workload)
+    if not entry:
+        return None
+    sha, traffic = entry
+    return traffic if sha == decode_sources_sha() else None
+
+
+def prefill_flops(shape, T):
+    """Algorithmic FLOPs of a T-position prefill: the four projections on every row, the
+    causal half of attention (query t attends to t + 1 keys: QK^T and PV, 2 FLOPs per MAC),
+    and the tied head on the last row only."""
+    H, D, F = shape.hidden, shape.head_dim, shape.ffn
+    linear = 2 * T * (shape.qkv_rows * H + H * shape.n_q_heads * D + 2 * F * H + H * F)
+    attn = 2 * 2 * D * shape.n_q_heads * (T * (T + 1) // 2)
+    return shape.n_layers * (linear + attn) + 2 * shape.vocab * H
+
+
+def time_long_prefill(w, stream, dev, reps=7, warmup=3):
+    """The 4096-position prefill of the long-context workload (32 ids, 4032 audio rows, 32
+    ids), replayed from its CUDA graph after the first two runs; CUDA events on the
+    decoder's stream, median of `reps`.  Returns (median ms, all ms)."""
+    import torch
+    from qwen3_prefill_kv_gb300 import synth, _lib
+    wl = synth.WORKLOADS["long_context"]
+    p = synth.make_prompt(wl, seed=0)
+    audio = p.audio.to(dev)
+    dec = _lib.Decoder(wl.shape, w, max_seq=wl.n_prompt, stream=stream)
+    for _ in range(warmup):
+        dec.prefill(p.ids, audio, p.audio_offset, want_argmax=False)
+    ms = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        dec.prefill(p.ids, audio, p.audio_offset, want_argmax=False)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms.append(e0.elapsed_time(e1))
+    dec.sync()
+    dec.close()
+    return statistics.median(ms), ms
 
 
 def decode_step_bytes(shape, L):
@@ -301,22 +359,26 @@ def run_ours(args):
         for _ in range(max(1, args.warmup)):
             step_host()
         torch.cuda.synchronize(dev)
-        e_dec = []
+        e_req = []
         for _ in range(args.steps):
-            t0 = time.perf_counter()
-            tok = dec.prefill(ids_h, audio_h, prompt.audio_offset)
-            t1 = time.perf_counter()
-            for j in range(wl.n_decode):
-                last = j == wl.n_decode - 1
-                tok = dec.decode_step(tok, logits=logits_h if last else None)
             torch.cuda.synchronize(dev)
-            e_dec.append(time.perf_counter() - t1)
-        h2d = ids.numel() * 4 + prompt.audio.numel() * 2 + wl.n_decode * 4
-        d2h = (wl.n_decode + 1) * 4 + shape.vocab * 4
-        e_total, = reduce_max_over_ranks([sum(e_dec)], world, dev)
-        e2e = {"value": whole_job_rate(world, wl.n_decode * len(e_dec), e_total), "unit": UNIT,
+            t0 = time.perf_counter()
+            step_host()
+            torch.cuda.synchronize(dev)
+            e_req.append(time.perf_counter() - t0)
+        # copied inside the interval, per request: the prompt ids and audio rows (host to
+        # device); the argmax with the step's error word after the prefill and after every
+        # decode step (8 bytes each), and the last step's logits (device to host).  Decode
+        # tokens travel as kernel arguments, not as copies.
+        h2d = ids.numel() * 4 + prompt.audio.numel() * 2
+        d2h = (wl.n_decode + 1) * 8 + shape.vocab * 4
+        e_total, = reduce_max_over_ranks([sum(e_req)], world, dev)
+        e2e = {"value": whole_job_rate(world, wl.n_decode * len(e_req), e_total), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_token": 1e3 * e_total / (wl.n_decode * len(e_dec))}
+               "ms_per_request": 1e3 * e_total / len(e_req),
+               "interval": ("whole request through the C ABI from pinned host buffers: prefill (ids and audio "
+                            "copied in), then the greedy decode steps with each argmax read back to the host and "
+                            "passed as the next token; value = generated tokens / interval")}
 
     dec_total_s = sum(dec_ms) / 1e3
     pre_total_s = sum(pre_ms) / 1e3
@@ -342,10 +404,21 @@ def run_ours(args):
                                     else "decode step (graph of the CUDA-core kernels of one token)"),
                          "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                          "peak_kind": peak_kind,
-                         "traffic": (PROFILED_DECODE_TRAFFIC.get(wl.name) if dec.decode_kernel == 0 else None),
+                         "traffic": (profiled_decode_traffic(wl.name) if dec.decode_kernel == 0 else None),
                          "algorithmic_bytes_per_launch": bytes_per_token},
             "clocks": clocks, "gpu_launches": int(launches) * world,
             "e2e": e2e}
+    if not args.no_long_prefill:
+        # the stated prefill target: the 4096-position prompt against the bf16 tensor peak
+        med, all_ms = time_long_prefill(w, stream, dev)
+        med, = reduce_max_over_ranks([med], world, dev)
+        fl = prefill_flops(shape, 4096)
+        ach = fl / (med * 1e-3) / 1e12
+        line["prefill_4096_ms"] = med
+        line["prefill_roofline"] = {"bound": "tensor", "workload": "long_context prefill (4096 positions)",
+                                    "flops": fl, "achieved": ach, "peak": bf16, "unit": "TFLOP/s",
+                                    "frac": ach / bf16, "peak_kind": f"{peak_kind} bf16 burst",
+                                    "ms_all": all_ms, "timing": "median of 7 graph replays, CUDA events"}
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         try:
             # the workload's own prefill and decode steps, repeated to about 10 s of oracle work

@@ -42,7 +42,7 @@ extern "C" {
 #define QDEC_E_CUDA         (-4)  /* a CUDA runtime/driver call failed (context may be unusable) */
 #define QDEC_E_OOM          (-5)  /* device or pinned allocation failed */
 #define QDEC_E_TIMEOUT      (-6)  /* a bounded device-side wait gave up (error flag set by a kernel);
-                                       the step's outputs and the KV slot it wrote are invalid */
+                                       the step's outputs are invalid; see qdec_decode_step */
 #define QDEC_E_UNSUPPORTED  (-7)  /* model shape outside what the kernels implement */
 
 /* Model shape.  Qwen3-0.6B: hidden 1024, 28 layers, 16 q heads, 8 kv heads,
@@ -78,7 +78,10 @@ typedef struct {
 
 typedef struct qdec_ctx qdec_ctx;
 
-/* Creates a context: validates the shape, records the weight pointers,
+/* Creates a context ("Fun-ASR-Nano Native Runtime Implementation Plan",
+ * Task 1 Step 1 fixes the shape tuple; Task 3 keeps the weights as
+ * non-owning tensors; "Qwen3ASR ncnn多平台移植" §5 holds a generation's state in
+ * a context object): validates the shape, records the weight pointers,
  * allocates the KV cache [n_layers][2][n_kv_heads][max_seq][head_dim] bf16,
  * the decode scratch and a RoPE cos/sin table [max_seq][head_dim/2] (angles
  * p * theta^(-2i/D) evaluated in double on the host, stored as fp32).
@@ -110,11 +113,20 @@ int qdec_prefill(qdec_ctx *ctx, const int32_t *ids, int32_t n_ids,
  * == -1 feeds back the previous step's argmax without a host round trip.
  * Writes KV slot n, advances the position by one, evaluates the lm_head.
  * logits_out / argmax_out as in qdec_prefill.  Errors: STATE (no prefill),
- * CAPACITY (n >= max_seq), INVALID_ARG (token < -1 or >= vocab). */
+ * CAPACITY (n >= max_seq), INVALID_ARG (token < -1 or >= vocab), TIMEOUT (a
+ * wait of the persistent step gave up, QDEC_OPT_SPIN_LIMIT).  A TIMEOUT
+ * reported by this call (argmax_out given) leaves the position, the device
+ * argmax and slots [0, n) as they were, so the step can be run again with the
+ * same token (pass it explicitly when the context samples); a TIMEOUT that
+ * surfaces later through qdec_sync needs a new prefill. */
 int qdec_decode_step(qdec_ctx *ctx, int32_t token, float *logits_out, int32_t *argmax_out);
 
 /* One lockstep decode step for n contexts (clones of one prefill or
- * independent prompts) sharing weights and shape.  tokens: HOST int32 [n]
+ * independent prompts) sharing weights and shape.  The pages run one
+ * context at a time ("Qwen3ASR ncnn多平台移植" §1 lists no batch inference);
+ * this call is each context's step of §5 taken together for the branching
+ * workload (one 415-position prefill cloned into 64 streams), so each stream
+ * computes exactly its own single-context step.  tokens: HOST int32 [n]
  * (-1 = previous argmax of that context).  logits_out: NULL or fp32
  * [n, vocab] (host or device); argmax_out: NULL or HOST int32 [n].  Each
  * context advances by one.  Errors as qdec_decode_step, plus STATE when the
@@ -129,7 +141,9 @@ int qdec_decode_step_batch(qdec_ctx *const *ctxs, int32_t n, const int32_t *toke
 int qdec_clone(const qdec_ctx *src, qdec_ctx **out);
 
 /* Number of positions written (prompt + decoded tokens); 0 before prefill;
- * a negative code for a NULL context. */
+ * a negative code for a NULL context.  This is n_past of "Forward map -
+ * funasr_nano", Generation / KV Path (decode runs at n_past >= T_prompt), the
+ * position counter of the context in "Qwen3ASR ncnn多平台移植" §5. */
 int qdec_position(const qdec_ctx *ctx);
 
 /* Copies KV slots [pos0, pos0 + n_pos) of one layer to HOST memory as bf16
@@ -161,6 +175,14 @@ int qdec_sync(const qdec_ctx *ctx);
                                         kv head merges them): 0 = the library default (one unit
                                         up to 160 keys, else about 64 keys per unit), or
                                         8 .. 4096 in multiples of 8 */
+#define QDEC_OPT_SPIN_LIMIT      5   /* how long each wait of the persistent decode step polls
+                                        (ring-stage barriers, tagged hand-off vectors) before it
+                                        gives up and the step reports QDEC_E_TIMEOUT: 0 = the
+                                        library default (2^21 polls, about a second), or a
+                                        positive count.  Small values make waits that are not
+                                        satisfied almost at once give up: a way to exercise the
+                                        timeout path without any fault.  The kernel's final wait
+                                        for its own copies in flight keeps the default. */
 
 /* Sets an option.  QDEC_OPT_DECODE_KERNEL = QDEC_DECODE_PERSISTENT returns
  * UNSUPPORTED when the persistent kernel does not cover the shape (head_dim /
@@ -208,10 +230,14 @@ int qdec_set_sampling(qdec_ctx *ctx, float temperature, int32_t top_k, float top
  * capacity >= that number), synchronises and returns the number. */
 int qdec_read_trace(const qdec_ctx *ctx, uint64_t *host_dst, int32_t capacity);
 
-/* Frees the context (KV cache, scratch, graphs).  NULL is a no-op. */
+/* Frees the context (KV cache, scratch, graphs) — the end of a context's
+ * life in "Qwen3ASR ncnn多平台移植" §5.  Waits for the context's queued work
+ * first.  NULL is a no-op. */
 void qdec_destroy(qdec_ctx *ctx);
 
-/* Static description of a status code. */
+/* Static description of a status code.  The pages give their C/C++ calls no
+ * error convention ("Qwen3ASR ncnn多平台移植" §5 names the steps only); the
+ * codes above are this library's. */
 const char *qdec_strerror(int status);
 
 /* Message of the most recent failure on the calling thread ("" if none). */

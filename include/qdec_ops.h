@@ -98,7 +98,9 @@ int qdec_op_lm_head_argmax(const void *E, int32_t V, int32_t H, const float *x, 
  * holds until the process exits.  The paper has no counterpart of this call.
  * The caller still passes inputs and outputs (as for qdec_op_lm_head_argmax).
  * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  Each call
+ * device current); make that first call before any stream capture.  The
+ * address is kept for the life of the process: after cudaDeviceReset on a
+ * device, this call is no longer valid there.  Each call
  * clears the ticket counter on `stream` before its kernel.  All calls share
  * the one array, so calls that overlap on the GPU (different streams, or other
  * host threads) race and give wrong results: serialise them.  Errors:

@@ -188,6 +188,7 @@ struct qdec_ctx {
     unsigned long long* d_trace = nullptr;   // phase trace of the persistent step (QDEC_OPT_TRACE)
     int prefill_gemm = QDEC_PREFILL_TCGEN05;
     int attn_unit_keys = 0;      // QDEC_OPT_ATTN_UNIT_KEYS (0 = default)
+    int spin_limit = 0;          // QDEC_OPT_SPIN_LIMIT (0 = default)
     // token choice (qdec_set_sampling); greedy while temperature is 0 and penalty 1
     float samp_t = 0.f, samp_p = 1.f, samp_r = 1.f;
     int samp_k = 0;
@@ -546,6 +547,7 @@ int enqueue_decode_step(qdec_ctx* c, int token) {
         p.am_part = c->am_part;
         p.am_count = c->am_count;
         p.err = c->d_err;
+        p.spin_limit = c->spin_limit > 0 ? (uint32_t)c->spin_limit : kDecodeSpinDefault;
         p.trace = c->d_trace;
         if (p.trace)
             CK(cudaMemsetAsync(p.trace, 0, (size_t)c->dp.grid * (11 * sh.NL + 8) * sizeof(unsigned long long),
@@ -955,8 +957,12 @@ int qdec_decode_step(qdec_ctx* c, int32_t token, float* logits_out, int32_t* arg
     c->position += 1;
     rc = copy_logits_out(c, logits_out);
     if (rc != QDEC_OK) return rc;
-    if (argmax_out) return sync_status(c, 0, argmax_out);
-    return QDEC_OK;
+    if (!argmax_out) return QDEC_OK;
+    rc = sync_status(c, 0, argmax_out);
+    // A step that gave up on a wait advanced nothing on the device (position, argmax); the
+    // host position follows, so the same step can be run again and rewrites its KV slot.
+    if (rc == QDEC_E_TIMEOUT) c->position -= 1;
+    return rc;
 }
 
 int qdec_decode_step_batch(qdec_ctx* const* ctxs, int32_t n, const int32_t* tokens, float* logits_out,
@@ -1020,6 +1026,7 @@ int qdec_clone(const qdec_ctx* src, qdec_ctx** out) {
     if (c->persistent_ok) c->decode_kernel = src->decode_kernel;
     c->prefill_gemm = src->prefill_gemm;
     c->attn_unit_keys = src->attn_unit_keys;
+    c->spin_limit = src->spin_limit;
     c->samp_t = src->samp_t; c->samp_p = src->samp_p; c->samp_r = src->samp_r; c->samp_k = src->samp_k;
     c->samp_seed = src->samp_seed;
     *out = c;
@@ -1073,6 +1080,11 @@ int qdec_set_option(qdec_ctx* c, int32_t option, int32_t value) {
         c->attn_unit_keys = value;
         return QDEC_OK;
     }
+    if (option == QDEC_OPT_SPIN_LIMIT) {
+        if (value < 0) return fail(QDEC_E_INVALID_ARG, "QDEC_OPT_SPIN_LIMIT takes 0 (default) or a positive count");
+        c->spin_limit = value;
+        return QDEC_OK;
+    }
     if (option == QDEC_OPT_TRACE) {
         if (value != 0 && value != 1) return fail(QDEC_E_INVALID_ARG, "QDEC_OPT_TRACE takes 0 or 1");
         if (value == 1 && !c->persistent_ok) return fail(QDEC_E_UNSUPPORTED, "no persistent decode kernel to trace");
@@ -1115,6 +1127,7 @@ int qdec_get_option(const qdec_ctx* c, int32_t option) {
     if (option == QDEC_OPT_TRACE) return c->d_trace ? 1 : 0;
     if (option == QDEC_OPT_PREFILL_IMPL) return c->prefill_gemm;
     if (option == QDEC_OPT_ATTN_UNIT_KEYS) return c->attn_unit_keys;
+    if (option == QDEC_OPT_SPIN_LIMIT) return c->spin_limit;
     if (option != QDEC_OPT_DECODE_KERNEL) return fail(QDEC_E_INVALID_ARG, "unknown option %d", option);
     return c->decode_kernel;
 }

@@ -207,8 +207,12 @@ struct DecodeParams {
     ArgMax* am_part;                    // [grid]
     unsigned int* am_count;             // zero between steps
     int* err;                           // 0, or the first error code of the step
+    uint32_t spin_limit;                // polls / barrier tests before a wait gives up
     unsigned long long* trace;          // optional [grid][11 NL + 4] globaltimer stamps, or null
 };
+
+// Default of DecodeParams::spin_limit: about a second of polls before a wait gives up.
+constexpr uint32_t kDecodeSpinDefault = 1u << 21;
 
 struct DecodeLaunch {
     const void* fn = nullptr;

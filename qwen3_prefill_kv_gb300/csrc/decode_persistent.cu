@@ -39,7 +39,9 @@ constexpr uint32_t SLOT = 16384;          // ring slot bytes
 constexpr int MAX_PR = (3072 / 2 + NCT - 1) / NCT;   // tagged word pairs per consumer thread (n <= 3072)
 constexpr int PB = 4;                     // polls a thread keeps in flight (registers: 4 per pair)
 constexpr uint32_t SPIN_FAST = 256;       // tagged-vector polls before backing off with nanosleep
-constexpr uint32_t SPIN_LIMIT = 1u << 21; // polls (each ~0.3-1 us) before a wait gives up: about a second
+constexpr uint32_t SPIN_LIMIT = kDecodeSpinDefault; // default polls (each ~0.3-1 us) before a wait gives up: about a
+                                          // second; DecodeParams::spin_limit carries the step's own limit, and
+                                          // the exit drain of copies in flight always uses this one
 enum { PH_QKV = 0, PH_O = 1, PH_X1 = 2, PH_H = 3, PH_X2 = 4, PH_PER_LAYER = 5 };
 enum { ERR_LL = 1, ERR_FULL = 2, ERR_EMPTY = 3, ERR_DRAIN = 4, ERR_PEER = 5 };
 enum { F_ABORT = 0, F_ISSUED = 1 };
@@ -288,7 +290,7 @@ __device__ inline bool should_abort(const Ctx& S, const DecodeParams& p, bool ch
 __device__ inline bool wait_bar(const Ctx& S, const DecodeParams& p, uint64_t* bar, uint32_t parity, int code) {
     if (mbar_test_wait(bar, parity)) return true;
     if (reinterpret_cast<volatile int*>(S.flags)[F_ABORT]) return false;
-    for (uint32_t it = 0; it < SPIN_LIMIT; ++it) {
+    for (uint32_t it = 0; it < p.spin_limit; ++it) {
         if (mbar_try_wait(bar, parity)) return true;   // suspends the thread for a while when not ready
         if ((it & 1023) == 1023 && should_abort(S, p, (it & 16383) == 16383)) return false;
     }
@@ -361,7 +363,7 @@ __device__ __forceinline__ bool ll_fetch(const Ctx& S, const DecodeParams& p, co
             }
         }
         if (!pending) break;
-        if (it >= SPIN_LIMIT) {
+        if (it >= p.spin_limit) {
             raise_error(S, p, ERR_LL);
             return false;
         }

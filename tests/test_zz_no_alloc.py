@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from qwen3_prefill_kv_gb300 import _lib
 
 pytestmark = pytest.mark.gpu
@@ -41,6 +42,35 @@ def test_static_matches_scratch_entry_point_twice(V, H):
         got = logits.cpu().double().numpy()
         assert np.abs(got - ref).max() <= 1e-4 * np.abs(ref).max(), f"call {call}: logits differ"
         assert int(am.item()) == int(ref_am.item()) == int(np.argmax(got)), f"call {call}: argmax differs"
+        # and against the float64 oracle on the same bf16 inputs (final RMSNorm, then E . h)
+        f64 = lambda t: t.cpu().to(torch.float64).numpy()
+        z = oracle.tied_lm_head(f64(E), oracle.rms_norm(f64(x), f64(gf), 1e-6))
+        assert np.abs(got - z).max() <= 1e-4 * np.abs(z).max(), f"call {call}: logits differ from the oracle"
+
+
+def test_static_serialised_calls_on_two_streams():
+    """Calls on different streams share the one static array; ordered by an event, a call on a
+    second stream still starts from a cleared ticket and gives the oracle's logits and argmax."""
+    V, H = 151936, 1024
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    prev = torch.cuda.current_stream()
+    for k, st in enumerate((s1, s2, s1)):
+        E, x, gf = _inputs(V, H, 20 + k)
+        logits = torch.empty(V, device="cuda")
+        am = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+        st.wait_stream(torch.cuda.current_stream())   # the inputs are written
+        st.wait_stream(prev)                          # the previous call is done with the array
+        _lib.lm_head_argmax_static(E, V, H, x, gf, 1e-6, logits, am, stream=st)
+        prev = st
+        outs.append((E, x, gf, logits, am, st))
+    torch.cuda.synchronize()
+    for k, (E, x, gf, logits, am, st) in enumerate(outs):
+        f64 = lambda t: t.cpu().to(torch.float64).numpy()
+        z = oracle.tied_lm_head(f64(E), oracle.rms_norm(f64(x), f64(gf), 1e-6))
+        got = logits.cpu().double().numpy()
+        assert np.abs(got - z).max() <= 1e-4 * np.abs(z).max(), k
+        assert int(am.item()) == int(np.argmax(got)), k
 
 
 def test_static_rejects_vocab_beyond_maximum():
