@@ -136,7 +136,7 @@ def test_decoder_sampling_trajectory(tiny, kernel):
     p = _prompt()
     T = p.ids.numel()
     t, k, pp, r, seed = 0.9, 50, 0.95, 1.2, 12345
-    dec = Decoder(synth.TINY, wd, max_seq=T + 10)
+    dec = Decoder(synth.TINY, wd, max_seq=T + 20)
     dec.decode_kernel = kernel
     dec.set_sampling(t, k, pp, r, seed)
     lg = torch.empty(synth.TINY.vocab, device="cuda")
