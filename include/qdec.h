@@ -184,6 +184,13 @@ int qdec_sync(const qdec_ctx *ctx);
                                         timeout path without any fault.  The kernel's final wait
                                         for its own copies in flight keeps the default. */
 
+#define QDEC_OPT_SHARED_PREFIX   7   /* 1 (default): in qdec_decode_step_batch, contexts cloned
+                                        from one prefill attend the prompt positions they hold
+                                        in common once for all of them (read from one member's
+                                        cache), and only their own positions past it per
+                                        context; 0: every context attends over its own copy.
+                                        Read from the batch's first context. */
+
 /* Sets an option.  QDEC_OPT_DECODE_KERNEL = QDEC_DECODE_PERSISTENT returns
  * UNSUPPORTED when the persistent kernel does not cover the shape (head_dim /
  * GQA group / ffn combination) or the device (cooperative launch with one

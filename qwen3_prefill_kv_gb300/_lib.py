@@ -25,6 +25,7 @@ OPT_TRACE = 2
 OPT_PREFILL_IMPL = 3
 OPT_ATTN_UNIT_KEYS = 4
 OPT_SPIN_LIMIT = 5
+OPT_SHARED_PREFIX = 7
 PREFILL_TCGEN05, PREFILL_SIMT = 0, 1
 DECODE_PERSISTENT, DECODE_GRAPH = 0, 1
 IMPL_SIMT, IMPL_TCGEN05 = 0, 1

@@ -4,6 +4,8 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
+#include <map>
 #include <memory>
 #include <string>
 #include <vector>
@@ -16,6 +18,7 @@ using namespace qdec;
 namespace {
 
 thread_local std::string g_last_error;
+std::atomic<unsigned long long> g_prefix_ids{0};
 
 int fail(int code, const char* fmt, ...) {
     char buf[512];
@@ -87,6 +90,13 @@ struct BatchWork {
           *logits = nullptr;
     bf16_t *Xn = nullptr, *attn = nullptr, *h = nullptr;
     int* h_tokens = nullptr;             // pinned staging of the step's tokens, two buffers of cap
+    // shared prefixes of the composition: blocks of member streams that attend a common
+    // [0, P) once (PrefixItem), and the prefix ids / setting the table was built for
+    PrefixItem* d_items = nullptr;
+    int* d_members = nullptr;
+    int n_items = 0, max_chunks = 0, split_cap = 0;
+    std::vector<unsigned long long> member_prefix;
+    int shared_setting = -1;
     cudaEvent_t tok_ev[2] = {nullptr, nullptr};   // each buffer's upload
     int tok_slot = 0;
     int n_split = 1;
@@ -104,7 +114,8 @@ struct BatchWork {
     }
     void release() {
         drop_graph();
-        void* ps[] = {d_streams, d_tokens, d_am, X, qkv, q, part_ml, part_o, gu, logits, Xn, attn, h};
+        void* ps[] = {d_streams, d_tokens, d_am, X, qkv, q, part_ml, part_o, gu, logits, Xn, attn, h, d_items,
+                      d_members};
         for (void* p : ps)
             if (p) cudaFree(p);
         if (h_am) cudaFreeHost(h_am);
@@ -189,6 +200,12 @@ struct qdec_ctx {
     int prefill_gemm = QDEC_PREFILL_TCGEN05;
     int attn_unit_keys = 0;      // QDEC_OPT_ATTN_UNIT_KEYS (0 = default)
     int spin_limit = 0;          // QDEC_OPT_SPIN_LIMIT (0 = default)
+    int shared_prefix = 1;       // QDEC_OPT_SHARED_PREFIX
+    // Which prefill this context's KV prefix comes from, and how many of its positions came from
+    // it: a prefill takes a new id and inherits its prompt; a clone keeps both.  Positions below
+    // `inherited` are never rewritten, so contexts with one id hold the same [0, inherited).
+    unsigned long long prefix_id = 0;
+    int inherited = 0;
     // token choice (qdec_set_sampling); greedy while temperature is 0 and penalty 1
     float samp_t = 0.f, samp_p = 1.f, samp_r = 1.f;
     int samp_k = 0;
@@ -616,25 +633,65 @@ int ensure_batch_work(qdec_ctx* const* ctxs, int n) {
         CK(dalloc(&b.Xn, (size_t)n * sh.H));
         CK(dalloc(&b.qkv, (size_t)n * sh.qkv_rows()));
         CK(dalloc(&b.q, (size_t)n * qd));
-        CK(dalloc(&b.part_ml, (size_t)n * sh.HQ * b.n_split * 2));
-        CK(dalloc(&b.part_o, (size_t)n * sh.HQ * b.n_split * sh.D));
+        b.split_cap = b.n_split + (prefix_attention_supported(sh) ? prefix_chunks(sh.max_seq) : 0);
+        CK(dalloc(&b.part_ml, (size_t)n * sh.HQ * b.split_cap * 2));
+        CK(dalloc(&b.part_o, (size_t)n * sh.HQ * b.split_cap * sh.D));
+        CK(dalloc(&b.d_members, (size_t)n));
+        CK(dalloc(&b.d_items, (size_t)n));
         CK(dalloc(&b.attn, (size_t)n * qd));
         CK(dalloc(&b.gu, (size_t)n * 2 * sh.F));
         CK(dalloc(&b.h, (size_t)n * sh.F));
         CK(dalloc(&b.logits, (size_t)n * sh.V));
         b.cap = n;
     }
-    bool same = (int)b.members.size() == n;
-    for (int i = 0; same && i < n; ++i) same = b.members[i] == ctxs[i];
+    const int want_shared = (c0->shared_prefix && prefix_attention_supported(sh)) ? 1 : 0;
+    bool same = (int)b.members.size() == n && b.shared_setting == want_shared;
+    for (int i = 0; same && i < n; ++i) same = b.members[i] == ctxs[i] && b.member_prefix[i] == ctxs[i]->prefix_id;
     if (!same) {
         b.drop_graph();
-        std::vector<BatchStream> hs(n);
         b.members.assign(ctxs, ctxs + n);
+        b.member_prefix.resize(n);
+        for (int i = 0; i < n; ++i) b.member_prefix[i] = ctxs[i]->prefix_id;
+        b.shared_setting = want_shared;
+        // streams grouped by the prefill their prefix comes from; a group of two or more shares
+        // [0, P) with P the smallest inherited length among its members
+        std::vector<int> shared(n, 0), members;
+        std::vector<PrefixItem> items;
+        int max_chunks = 0;
+        if (want_shared) {
+            std::map<unsigned long long, std::vector<int>> groups;
+            for (int i = 0; i < n; ++i)
+                if (ctxs[i]->prefix_id != 0 && ctxs[i]->inherited > 0) groups[ctxs[i]->prefix_id].push_back(i);
+            const int per_item = prefix_item_streams(sh);
+            for (auto& kv : groups) {
+                const std::vector<int>& g = kv.second;
+                if (g.size() < 2) continue;
+                int P = ctxs[g[0]]->inherited;
+                for (int i : g) P = ctxs[i]->inherited < P ? ctxs[i]->inherited : P;
+                for (size_t a = 0; a < g.size(); a += per_item) {
+                    const int cnt = (int)(g.size() - a) < per_item ? (int)(g.size() - a) : per_item;
+                    items.push_back(PrefixItem{ctxs[g[0]]->kv, P, (int)members.size(), cnt});
+                    for (int k = 0; k < cnt; ++k) members.push_back(g[a + k]);
+                }
+                for (int i : g) shared[i] = P;
+                max_chunks = prefix_chunks(P) > max_chunks ? prefix_chunks(P) : max_chunks;
+            }
+        }
+        if (b.n_split + max_chunks > b.split_cap) return fail(QDEC_E_UNSUPPORTED, "shared prefix longer than max_seq");
+        b.n_items = (int)items.size();
+        b.max_chunks = max_chunks;
+        std::vector<BatchStream> hs(n);
         for (int i = 0; i < n; ++i)
             hs[i] = BatchStream{ctxs[i]->kv, ctxs[i]->d_pos, ctxs[i]->d_argmax, ctxs[i]->d_hist, ctxs[i]->rope,
-                                ctxs[i]->sh.max_seq};
+                                ctxs[i]->sh.max_seq, shared[i]};
         CK(cudaMemcpyAsync(b.d_streams, hs.data(), n * sizeof(BatchStream), cudaMemcpyHostToDevice, c0->stream));
-        CK(cudaStreamSynchronize(c0->stream));   // hs is pageable host memory that goes out of scope
+        if (!items.empty()) {
+            CK(cudaMemcpyAsync(b.d_items, items.data(), items.size() * sizeof(PrefixItem), cudaMemcpyHostToDevice,
+                               c0->stream));
+            CK(cudaMemcpyAsync(b.d_members, members.data(), members.size() * sizeof(int), cudaMemcpyHostToDevice,
+                               c0->stream));
+        }
+        CK(cudaStreamSynchronize(c0->stream));   // host vectors go out of scope
     }
     return QDEC_OK;
 }
@@ -669,7 +726,8 @@ int batch_body(qdec_ctx* c0, int n, cudaStream_t s, uint64_t* kernels) {
         CK(launch_rmsnorm_bf16(b.X, n, sh.H, w.g_in, sh.eps, b.Xn, s));
         if ((rc = batch_gemm(c0, b.Xn, sh.H, w.wqkv, n, sh.qkv_rows(), sh.H, false, b.qkv, sh.qkv_rows(), s))) return rc;
         CK(launch_batch_qk_rope(b.qkv, sh, l, w.g_q, w.g_k, b.d_streams, n, b.q, s));
-        CK(launch_batch_attention(b.q, sh, l, b.d_streams, n, b.n_split, b.part_ml, b.part_o, b.attn, s));
+        CK(launch_batch_attention(b.q, sh, l, b.d_streams, n, b.n_split, b.d_items, b.n_items, b.d_members,
+                                  b.max_chunks, b.part_ml, b.part_o, b.attn, s));
         if ((rc = batch_gemm(c0, b.attn, qd, w.wo, n, sh.H, qd, true, b.X, sh.H, s))) return rc;
         CK(launch_rmsnorm_bf16(b.X, n, sh.H, w.g_post, sh.eps, b.Xn, s));
         if ((rc = batch_gemm(c0, b.Xn, sh.H, w.wgu, n, 2 * sh.F, sh.H, false, b.gu, 2 * sh.F, s))) return rc;
@@ -938,6 +996,8 @@ int qdec_prefill(qdec_ctx* c, const int32_t* ids, int32_t n_ids, const void* aud
     count_launches(kernels);
     c->position = T;
     c->prefilled = true;
+    c->prefix_id = ++g_prefix_ids;
+    c->inherited = T;
     rc = copy_logits_out(c, logits_out);
     if (rc != QDEC_OK) return rc;
     if (argmax_out) return sync_status(c, 0, argmax_out);
@@ -1027,6 +1087,9 @@ int qdec_clone(const qdec_ctx* src, qdec_ctx** out) {
     c->prefill_gemm = src->prefill_gemm;
     c->attn_unit_keys = src->attn_unit_keys;
     c->spin_limit = src->spin_limit;
+    c->shared_prefix = src->shared_prefix;
+    c->prefix_id = src->prefix_id;
+    c->inherited = src->inherited < src->position ? src->inherited : src->position;
     c->samp_t = src->samp_t; c->samp_p = src->samp_p; c->samp_r = src->samp_r; c->samp_k = src->samp_k;
     c->samp_seed = src->samp_seed;
     *out = c;
@@ -1080,6 +1143,11 @@ int qdec_set_option(qdec_ctx* c, int32_t option, int32_t value) {
         c->attn_unit_keys = value;
         return QDEC_OK;
     }
+    if (option == QDEC_OPT_SHARED_PREFIX) {
+        if (value != 0 && value != 1) return fail(QDEC_E_INVALID_ARG, "QDEC_OPT_SHARED_PREFIX takes 0 or 1");
+        c->shared_prefix = value;
+        return QDEC_OK;
+    }
     if (option == QDEC_OPT_SPIN_LIMIT) {
         if (value < 0) return fail(QDEC_E_INVALID_ARG, "QDEC_OPT_SPIN_LIMIT takes 0 (default) or a positive count");
         c->spin_limit = value;
@@ -1128,6 +1196,7 @@ int qdec_get_option(const qdec_ctx* c, int32_t option) {
     if (option == QDEC_OPT_PREFILL_IMPL) return c->prefill_gemm;
     if (option == QDEC_OPT_ATTN_UNIT_KEYS) return c->attn_unit_keys;
     if (option == QDEC_OPT_SPIN_LIMIT) return c->spin_limit;
+    if (option == QDEC_OPT_SHARED_PREFIX) return c->shared_prefix;
     if (option != QDEC_OPT_DECODE_KERNEL) return fail(QDEC_E_INVALID_ARG, "unknown option %d", option);
     return c->decode_kernel;
 }

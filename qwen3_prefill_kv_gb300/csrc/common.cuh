@@ -165,13 +165,31 @@ struct BatchStream {        // one context of a lockstep batch
     int* hist;              // its token history
     const float2* rope;     // its RoPE table
     int max_seq;
+    int shared;             // keys [0, shared) are attended by the shared-prefix kernel (0 = none)
+};
+// A block of streams whose caches hold the same keys and values at [0, P) (clones of one
+// prefill): members[first .. first + count) are their indices in the batch; kv is one member's
+// cache, from which the prefix is read once for all of them.
+struct PrefixItem {
+    const bf16_t* kv;
+    int P, first, count;
 };
 cudaError_t launch_batch_embed(const bf16_t* E, int H, const int* tokens, const BatchStream* bs, int n, float* X,
                                cudaStream_t st);
 cudaError_t launch_batch_qk_rope(const float* qkv, const Shape& sh, int layer, const bf16_t* g_q, const bf16_t* g_k,
                                  const BatchStream* bs, int n, float* q_out, cudaStream_t st);
+// Attention of every stream over its keys [shared, L) in n_split splits, plus (n_items > 0) the
+// shared prefixes in max_chunks further splits, all merged into bf16 out [n, HQ * D].
 cudaError_t launch_batch_attention(const float* q, const Shape& sh, int layer, const BatchStream* bs, int n, int n_split,
+                                   const PrefixItem* items, int n_items, const int* members, int max_chunks,
                                    float* part_ml, float* part_o, bf16_t* out, cudaStream_t st);
+// Shared-prefix attention (k_batch_prefix.cu): head_dim 128 and a GQA group of 1, 2, 4 or 8.
+bool prefix_attention_supported(const Shape& sh);
+int prefix_item_streams(const Shape& sh);   // streams one PrefixItem may hold
+int prefix_chunks(int P);                   // key chunks of a prefix of P positions
+cudaError_t launch_prefix_attention(const float* q, const Shape& sh, int layer, const PrefixItem* items, int n_items,
+                                    const int* members, int max_chunks, int n_split_total, int split0, float* part_ml,
+                                    float* part_o, cudaStream_t st);
 // h = silu(g) * u from gu [n, 2F] (gate, then up), or from the sum of `splits` partial slabs of
 // it pstride floats apart.
 cudaError_t launch_batch_swiglu(const float* gu, int F, int n, bf16_t* h, cudaStream_t st, int splits = 1,

@@ -100,15 +100,17 @@ __device__ __forceinline__ void row_lane(const bf16_t* row, int lane, float (&ou
     }
 }
 
-// Split-KV attention of one stream's kv head over its keys [0, pos + 1).
-// grid (HKV, n_split, n); partials [n][HQ][n_split] (m, l) and (o[D]), m in log2 units.
+// Split-KV attention of one stream's kv head over its keys [shared, pos + 1).
+// grid (HKV, n_split, n); partials [n][HQ][n_split_total] (m, l) and (o[D]), m in log2 units:
+// splits [0, n_split) here, the rest written by the shared-prefix kernel.
 // Each warp takes groups of BP positions: their K/V loads are all in flight together, the
 // BP x G scores are reduced across the warp together, then one online-softmax update
 // (exp2 of scores pre-scaled by log2(e)/sqrt(D)) folds the group in.
 template <int D, int G>
 __global__ void __launch_bounds__(BNT) batch_attn_kernel(const float* __restrict__ q, int HQ, int HKV, int layer,
                                                          const BatchStream* __restrict__ bs, int n_split,
-                                                         float* __restrict__ part_ml, float* __restrict__ part_o) {
+                                                         int n_split_total, float* __restrict__ part_ml,
+                                                         float* __restrict__ part_o) {
     constexpr int EPL = D / 32;
     __shared__ float sm[BWARPS][G];
     __shared__ float sl[BWARPS][G];
@@ -117,8 +119,8 @@ __global__ void __launch_bounds__(BNT) batch_attn_kernel(const float* __restrict
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const BatchStream st = bs[s];
     const int L = *st.pos + 1;
-    const int chunk = (L + n_split - 1) / n_split;
-    const int j0 = split * chunk, j1 = min(L, j0 + chunk);
+    const int chunk = (L - st.shared + n_split - 1) / n_split;   // this stream's own keys [shared, L)
+    const int j0 = st.shared + split * chunk, j1 = min(L, j0 + chunk);
     const size_t layer_stride = (size_t)2 * HKV * st.max_seq * D;
     const bf16_t* kb = st.kv + (size_t)layer * layer_stride + (size_t)gk * st.max_seq * D;
     const bf16_t* vb = kb + (size_t)HKV * st.max_seq * D;
@@ -204,7 +206,7 @@ __global__ void __launch_bounds__(BNT) batch_attn_kernel(const float* __restrict
                 ot += f * so[w][gi][d];
             }
         }
-        const size_t base = ((size_t)s * HQ + gk * G + gi) * n_split + split;
+        const size_t base = ((size_t)s * HQ + gk * G + gi) * n_split_total + split;
         part_o[base * D + d] = ot;
         if (d == 0) {
             part_ml[base * 2 + 0] = M;
@@ -214,10 +216,14 @@ __global__ void __launch_bounds__(BNT) batch_attn_kernel(const float* __restrict
 }
 
 // Merge of the splits; writes the attention output bf16 [n, HQ * D] (the o_proj GEMM operand).
-__global__ void batch_attn_merge_kernel(int HQ, int D, int n_split, const float* __restrict__ part_ml,
+// A stream without a shared prefix has only its own n_split splits; one with a shared prefix
+// also has the prefix kernel's splits [n_split, n_split_total).
+__global__ void batch_attn_merge_kernel(int HQ, int D, int n_split_own, int n_split_total,
+                                        const BatchStream* __restrict__ bs, const float* __restrict__ part_ml,
                                         const float* __restrict__ part_o, bf16_t* __restrict__ out) {
     const int h = blockIdx.x, s = blockIdx.y;
-    const size_t base = ((size_t)s * HQ + h) * n_split;
+    const size_t base = ((size_t)s * HQ + h) * n_split_total;
+    const int n_split = bs[s].shared > 0 ? n_split_total : n_split_own;
     float M = -INFINITY;
     for (int k = 0; k < n_split; ++k) M = fmaxf(M, part_ml[(base + k) * 2]);
     for (int d = threadIdx.x; d < D; d += blockDim.x) {
@@ -297,13 +303,13 @@ __global__ void batch_argmax_kernel(const float* __restrict__ logits, int V, int
 
 template <int D>
 cudaError_t launch_attn_d(const float* q, int HQ, int HKV, int layer, const BatchStream* bs, int n, int n_split,
-                          float* part_ml, float* part_o, cudaStream_t st) {
+                          int nst, float* part_ml, float* part_o, cudaStream_t st) {
     dim3 grid(HKV, n_split, n);
     switch (HQ / HKV) {
-        case 1: batch_attn_kernel<D, 1><<<grid, BNT, 0, st>>>(q, HQ, HKV, layer, bs, n_split, part_ml, part_o); break;
-        case 2: batch_attn_kernel<D, 2><<<grid, BNT, 0, st>>>(q, HQ, HKV, layer, bs, n_split, part_ml, part_o); break;
-        case 4: batch_attn_kernel<D, 4><<<grid, BNT, 0, st>>>(q, HQ, HKV, layer, bs, n_split, part_ml, part_o); break;
-        case 8: batch_attn_kernel<D, 8><<<grid, BNT, 0, st>>>(q, HQ, HKV, layer, bs, n_split, part_ml, part_o); break;
+        case 1: batch_attn_kernel<D, 1><<<grid, BNT, 0, st>>>(q, HQ, HKV, layer, bs, n_split, nst, part_ml, part_o); break;
+        case 2: batch_attn_kernel<D, 2><<<grid, BNT, 0, st>>>(q, HQ, HKV, layer, bs, n_split, nst, part_ml, part_o); break;
+        case 4: batch_attn_kernel<D, 4><<<grid, BNT, 0, st>>>(q, HQ, HKV, layer, bs, n_split, nst, part_ml, part_o); break;
+        case 8: batch_attn_kernel<D, 8><<<grid, BNT, 0, st>>>(q, HQ, HKV, layer, bs, n_split, nst, part_ml, part_o); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -328,17 +334,23 @@ cudaError_t launch_batch_qk_rope(const float* qkv, const Shape& sh, int layer, c
 }
 
 cudaError_t launch_batch_attention(const float* q, const Shape& sh, int layer, const BatchStream* bs, int n, int n_split,
+                                   const PrefixItem* items, int n_items, const int* members, int max_chunks,
                                    float* part_ml, float* part_o, bf16_t* out, cudaStream_t st) {
     (void)cudaGetLastError();
+    const int nst = n_split + (n_items > 0 ? max_chunks : 0);
     cudaError_t e;
     switch (sh.D) {
-        case 32: e = launch_attn_d<32>(q, sh.HQ, sh.HKV, layer, bs, n, n_split, part_ml, part_o, st); break;
-        case 64: e = launch_attn_d<64>(q, sh.HQ, sh.HKV, layer, bs, n, n_split, part_ml, part_o, st); break;
-        case 128: e = launch_attn_d<128>(q, sh.HQ, sh.HKV, layer, bs, n, n_split, part_ml, part_o, st); break;
+        case 32: e = launch_attn_d<32>(q, sh.HQ, sh.HKV, layer, bs, n, n_split, nst, part_ml, part_o, st); break;
+        case 64: e = launch_attn_d<64>(q, sh.HQ, sh.HKV, layer, bs, n, n_split, nst, part_ml, part_o, st); break;
+        case 128: e = launch_attn_d<128>(q, sh.HQ, sh.HKV, layer, bs, n, n_split, nst, part_ml, part_o, st); break;
         default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
-    batch_attn_merge_kernel<<<dim3(sh.HQ, n), 128, 0, st>>>(sh.HQ, sh.D, n_split, part_ml, part_o, out);
+    if (n_items > 0) {
+        e = launch_prefix_attention(q, sh, layer, items, n_items, members, max_chunks, nst, n_split, part_ml, part_o, st);
+        if (e != cudaSuccess) return e;
+    }
+    batch_attn_merge_kernel<<<dim3(sh.HQ, n), 128, 0, st>>>(sh.HQ, sh.D, n_split, nst, bs, part_ml, part_o, out);
     return cudaGetLastError();
 }
 
