@@ -54,7 +54,8 @@ class QdecWeights(C.Structure):
 
 _lib = None
 
-# Every symbol include/qdec.h and include/qdec_ops.h declare: (name, restype, argtypes).
+# Every symbol include/qdec.h, include/qdec_ops.h and include/qdec_adaptor.h declare:
+# (name, restype, argtypes).
 _VP, _I32, _F, _SZ = C.c_void_p, C.c_int32, C.c_float, C.c_size_t
 SIGNATURES = [
     ("qdec_create", C.c_int, [C.POINTER(QdecConfig), C.POINTER(QdecWeights), _VP, C.POINTER(_VP)]),
@@ -83,6 +84,10 @@ SIGNATURES = [
     ("qdec_op_lm_head_scratch_bytes", _SZ, [_I32]),
     ("qdec_op_lm_head_argmax", C.c_int, [_VP, _I32, _I32, _VP, _VP, _F, _VP, _VP, _VP, _SZ, _VP]),
     ("qdec_op_lm_head_argmax_static", C.c_int, [_VP, _I32, _I32, _VP, _VP, _F, _VP, _VP, _VP]),
+    ("qdec_fake_token_len", C.c_int32, [_I32]),
+    ("qdec_adaptor_create", C.c_int, [_VP, _VP, _VP, C.POINTER(_VP)]),
+    ("qdec_adaptor_run", C.c_int, [_VP, _VP, _I32, _VP, _VP]),
+    ("qdec_adaptor_destroy", None, [_VP]),
 ]
 
 LM_HEAD_STATIC_MAX_VOCAB = 262144
@@ -314,3 +319,58 @@ def lm_head_argmax(E, V, H, x, g_final, eps, logits, argmax, scratch, stream=Non
     nbytes = scratch.numel() * scratch.element_size()
     _check(lib.qdec_op_lm_head_argmax(_ptr(E), V, H, _ptr(x), _ptr(g_final), float(eps), _ptr(logits),
                                       _ptr(argmax), _ptr(scratch), nbytes, _stream_handle(stream)))
+
+
+# ------------------------------------------------------------------ audio adaptor
+class QdecAdaptorConfig(C.Structure):
+    _fields_ = [("enc_dim", C.c_int32), ("proj_dim", C.c_int32), ("hidden", C.c_int32), ("n_heads", C.c_int32),
+                ("ffn", C.c_int32), ("n_blocks", C.c_int32), ("ln_eps", C.c_float)]
+
+
+class QdecAdaptorWeights(C.Structure):
+    _fields_ = [("w1", C.c_void_p), ("w2", C.c_void_p), ("b1", C.c_void_p), ("b2", C.c_void_p),
+                ("ln1_g", _PP), ("ln1_b", _PP), ("ln2_g", _PP), ("ln2_b", _PP),
+                ("wqkv", _PP), ("wo", _PP), ("fc1", _PP), ("fc2", _PP),
+                ("bqkv", _PP), ("bo", _PP), ("fc1_b", _PP), ("fc2_b", _PP)]
+
+
+def fake_token_len(n_frames: int) -> int:
+    """qdec_fake_token_len: rows the adaptor keeps for n_frames encoder frames."""
+    return int(load().qdec_fake_token_len(int(n_frames)))
+
+
+class Adaptor:
+    """The projector + bidirectional adaptor (include/qdec_adaptor.h) over borrowed device
+    weights: ``weights`` maps w1, b1, w2, b2 and ``blocks`` (a list of mappings with ln1_g,
+    ln1_b, wqkv, bqkv, wo, bo, ln2_g, ln2_b, fc1, fc1_b, fc2, fc2_b) to CUDA tensors (bf16
+    matrices, fp32 vectors); the object keeps them alive."""
+
+    def __init__(self, shape, weights, stream=None):
+        self.lib = load()
+        self.shape = shape
+        self.weights = weights
+        cfg = QdecAdaptorConfig(shape.enc_dim, shape.proj_dim, shape.hidden, shape.n_heads, shape.ffn,
+                                shape.n_blocks, shape.ln_eps)
+        nb = shape.n_blocks
+        keys = ("ln1_g", "ln1_b", "ln2_g", "ln2_b", "wqkv", "wo", "fc1", "fc2", "bqkv", "bo", "fc1_b", "fc2_b")
+        self._arrs = {k: (C.c_void_p * max(nb, 1))(*[b[k].data_ptr() for b in weights["blocks"]]) for k in keys}
+        w = QdecAdaptorWeights(weights["w1"].data_ptr(), weights["w2"].data_ptr(), weights["b1"].data_ptr(),
+                               weights["b2"].data_ptr(), *[C.cast(self._arrs[k], _PP) for k in keys])
+        h = C.c_void_p()
+        _check(self.lib.qdec_adaptor_create(C.byref(cfg), C.byref(w), _stream_handle(stream), C.byref(h)))
+        self.handle = h
+
+    def run(self, frames, rows_out) -> int:
+        """frames bf16 [T, enc_dim] (host or device) -> rows_out bf16 [fake_token_len(T), hidden]
+        (host or device); returns the row count."""
+        n = C.c_int32(0)
+        _check(self.lib.qdec_adaptor_run(self.handle, _ptr(frames), int(frames.shape[0]), _ptr(rows_out),
+                                         C.byref(n)))
+        return int(n.value)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            self.lib.qdec_adaptor_destroy(self.handle)
+            self.handle = None
+
+    __del__ = close

@@ -99,8 +99,11 @@ int gemm_tc_splits(int K, int splits);
 // setting.  Process-wide, not thread-safe: for tuning and tests.
 int set_gemm_tile_width(int bn);
 int gemm_tile_width();   // the current setting (0, 128 or 256)
+// bias (fp32 [N], optional) is added to every row and relu (0/1) clamps at zero, after the
+// accumulation, in the STORE_F32, ADD_F32 (C += acc + bias) and STORE_BF16 modes.
 cudaError_t launch_gemm_tc(const bf16_t* A, int lda, const bf16_t* W, int M, int N, int K, int mode, int up_off,
-                           float* Cf, bf16_t* Cb, int ldc, cudaStream_t s, int splits = 1);
+                           float* Cf, bf16_t* Cb, int ldc, cudaStream_t s, int splits = 1,
+                           const float* bias = nullptr, int relu = 0);
 // The packed QKV projection with the per-head epilogue fused (head_dim 128, one head per
 // 128-column tile): q heads -> RMSNorm(g_q) + NeoX RoPE at pos0 + row -> bf16 q [M][HQ][128];
 // k heads -> RMSNorm(g_k) + RoPE -> bf16 K cache slot pos0 + row; v heads -> bf16 V cache.
@@ -126,6 +129,11 @@ cudaError_t launch_qk_norm_rope_append(const float* qkv, int T, const Shape& sh,
                                        bf16_t* q_bf16, float* q_f32, bf16_t* k_cache, bf16_t* v_cache,
                                        cudaStream_t s, int splits = 1, size_t pstride = 0);
 
+// Bidirectional multi-head attention (the audio adaptor, head_dim 128, one kv head per q head):
+// every query row attends every key row of the clip.  Q, K, V bf16 views [T][heads][128] with
+// rows row_stride elements apart; O bf16 [T][heads * 128].
+cudaError_t launch_attention_bidir_tc(const bf16_t* Q, const bf16_t* K, const bf16_t* V, int row_stride, int T,
+                                      int heads, bf16_t* O, cudaStream_t s);
 // Prefill attention: Q bf16 [T, HQ, D] at positions pos0..pos0+T-1 over cache keys [0, pos0+T).
 cudaError_t launch_attention_prefill_simt(const bf16_t* Q, int T, const Shape& sh, int pos0,
                                           const bf16_t* k_cache, const bf16_t* v_cache,

@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(192, 1) attn_prefill_tc_kernel(const __grid_co
                                                                  const __grid_constant__ CUtensorMap tmK,
                                                                  const __grid_constant__ CUtensorMap tmV, int T,
                                                                  int HQ, int HKV, int pos0, bf16_t* __restrict__ O,
-                                                                 float scale_log2) {
+                                                                 float scale_log2, int causal) {
     extern __shared__ __align__(1024) char smem_raw[];
     char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     char* sQ = smem;                                  // 32 KB
@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(192, 1) attn_prefill_tc_kernel(const __grid_co
     const int h = blockIdx.y, g = h / (HQ / HKV);
     const int q0 = qtile * QT;
     const int L = pos0 + T;
-    const int kend = min(L, pos0 + q0 + QT);          // keys [0, kend) can be visible to this tile
+    const int kend = causal ? min(L, pos0 + q0 + QT) : L;   // keys [0, kend) can be visible to this tile
     const int nt = (kend + KT - 1) / KT;
 
     if (threadIdx.x == 0) {
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(192, 1) attn_prefill_tc_kernel(const __grid_co
         for (int j = 0; j < nt; ++j) {
             const int st = j & 1;
             // a tile wholly below the diagonal (every key visible to every row) needs no mask
-            const bool full = (j * KT + KT - 1 <= pos0 + q0) && (j * KT + KT <= L);
+            const bool full = (!causal || j * KT + KT - 1 <= pos0 + q0) && (j * KT + KT <= L);
             mb_wait(&B->s_full[st], (j >> 1) & 1, 20);
             tc_fence_after();
             const uint32_t sadr = tmem + lane_off + st * 128;
@@ -273,7 +273,7 @@ __global__ void __launch_bounds__(192, 1) attn_prefill_tc_kernel(const __grid_co
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
                         const int key = j * KT + 32 * c + k;
-                        if (key <= qpos && key < L) mx = fmaxf(mx, sv[k]);
+                        if ((!causal || key <= qpos) && key < L) mx = fmaxf(mx, sv[k]);
                     }
                 }
             }
@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(192, 1) attn_prefill_tc_kernel(const __grid_co
 #pragma unroll
                     for (int k = 0; k < 32; ++k) {
                         const int key = j * KT + 32 * c + k;
-                        const bool vis = key <= qpos && key < L && m_new != -INFINITY;
+                        const bool vis = (!causal || key <= qpos) && key < L && m_new != -INFINITY;
                         pv[k] = vis ? ex2(fmaf(sv[k], scale_log2, -m_new)) : 0.f;
                         lsum += pv[k];
                     }
@@ -813,7 +813,31 @@ cudaError_t launch_attention_prefill_tc(const bf16_t* Q, int T, const Shape& sh,
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    attn_prefill_tc_kernel<<<dim3(ntq, sh.HQ), 192, smem, s>>>(mq, mk, mv, T, sh.HQ, sh.HKV, pos0, O, scale_log2);
+    attn_prefill_tc_kernel<<<dim3(ntq, sh.HQ), 192, smem, s>>>(mq, mk, mv, T, sh.HQ, sh.HKV, pos0, O, scale_log2, 1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attention_bidir_tc(const bf16_t* Q, const bf16_t* K, const bf16_t* V, int row_stride, int T,
+                                      int heads, bf16_t* O, cudaStream_t s) {
+    (void)cudaGetLastError();
+    if (T <= 0 || heads <= 0 || row_stride % 8 != 0 || row_stride < heads * 128) return cudaErrorInvalidValue;
+    // Q, K and V are views [T][heads][128] with rows row_stride elements apart (the three column
+    // blocks of one fused projection); K and V are read as [heads][T][128] through the strides
+    CUtensorMap mq, mk, mv;
+    const uint64_t D = 128, rs = (uint64_t)row_stride * 2;
+    if (!make_map3(&mq, Q, D, (uint64_t)heads, (uint64_t)T, D * 2, rs, 1, QT)) return cudaErrorInvalidValue;
+    if (!make_map3(&mk, K, D, (uint64_t)T, (uint64_t)heads, rs, D * 2, KT, 1)) return cudaErrorInvalidValue;
+    if (!make_map3(&mv, V, D, (uint64_t)T, (uint64_t)heads, rs, D * 2, KT, 1)) return cudaErrorInvalidValue;
+    constexpr int smem = 7 * TILE_BYTES + 1024 + 256;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(attn_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const float scale_log2 = 1.4426950408889634f / sqrtf(128.f);
+    const int ntq = (T + QT - 1) / QT;
+    attn_prefill_tc_kernel<<<dim3(ntq, heads), 192, smem, s>>>(mq, mk, mv, T, heads, heads, 0, O, scale_log2, 0);
     return cudaGetLastError();
 }
 

@@ -169,7 +169,8 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
                                                          const __grid_constant__ CUtensorMap tmB, int M, int K,
                                                          int up_off, float* __restrict__ Cf,
                                                          bf16_t* __restrict__ Cb, int ldc, const QkvRopeEpi epi,
-                                                         int tiles_m, int tiles_n, int splits) {
+                                                         int tiles_m, int tiles_n, int splits,
+                                                         const float* __restrict__ bias, int relu) {
     extern __shared__ __align__(1024) char smem_raw[];
     char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     constexpr int A_BYTES = BM * BK * 2;
@@ -331,6 +332,18 @@ __global__ void __launch_bounds__(192, 1) gemm_tc_kernel(const __grid_constant__
                 for (int c0 = 0; c0 < BN; c0 += 32) {
                     float v[32];
                     tmem_ld32(taddr + c0, v);
+                    if (bias) {   // per-column bias (the adaptor's linear layers), then ReLU
+                        const float4* b4 = reinterpret_cast<const float4*>(bias + n0 + c0);
+#pragma unroll
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const float4 b = __ldg(b4 + jj);
+                            v[4 * jj] += b.x; v[4 * jj + 1] += b.y; v[4 * jj + 2] += b.z; v[4 * jj + 3] += b.w;
+                        }
+                    }
+                    if (relu) {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) v[k] = fmaxf(v[k], 0.f);
+                    }
                     if (row < M) {
                         if (MODE == GEMM_STORE_BF16) {
                             uint4* dst = reinterpret_cast<uint4*>(Cb + (size_t)row * ldc + n0 + c0);
@@ -403,7 +416,8 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 
 template <int BN, int MODE, int STAGES>
 cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N, int K, int up_off, float* Cf,
-                      bf16_t* Cb, int ldc, int splits, cudaStream_t s, const QkvRopeEpi& epi = QkvRopeEpi{}) {
+                      bf16_t* Cb, int ldc, int splits, cudaStream_t s, const QkvRopeEpi& epi = QkvRopeEpi{},
+                      const float* bias = nullptr, int relu = 0) {
     constexpr int smem = STAGES * (BM * BK * 2 + BN * BK * 2) + 1024 + 256;
     auto kern = gemm_tc_kernel<BN, MODE, STAGES>;
     static int resident = 0;   // CTAs of this instantiation that fit on the device at once
@@ -421,7 +435,7 @@ cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, int M, int N
     const int tiles_m = (M + BM - 1) / BM, tiles_n = N / tile_n;
     const long long units = (long long)tiles_m * tiles_n * splits;
     const int grid = (int)(units < resident ? units : resident);   // persistent: each CTA walks units
-    kern<<<grid, 192, smem, s>>>(ma, mb, M, K, up_off, Cf, Cb, ldc, epi, tiles_m, tiles_n, splits);
+    kern<<<grid, 192, smem, s>>>(ma, mb, M, K, up_off, Cf, Cb, ldc, epi, tiles_m, tiles_n, splits, bias, relu);
     return cudaGetLastError();
 }
 
@@ -479,9 +493,12 @@ bool gemm_tc_supported(int N, int K, int mode, int lda) {
 }
 
 cudaError_t launch_gemm_tc(const bf16_t* A, int lda, const bf16_t* W, int M, int N, int K, int mode, int up_off,
-                           float* Cf, bf16_t* Cb, int ldc, cudaStream_t s, int splits) {
+                           float* Cf, bf16_t* Cb, int ldc, cudaStream_t s, int splits, const float* bias, int relu) {
     (void)cudaGetLastError();
     if (!gemm_tc_supported(N, K, mode, lda) || M <= 0) return cudaErrorInvalidValue;
+    // a bias or ReLU applies to the plain store / add epilogues only
+    if ((bias || relu) && mode != GEMM_STORE_F32 && mode != GEMM_ADD_F32 && mode != GEMM_STORE_BF16)
+        return cudaErrorInvalidValue;
     // each split needs at least one k-block; only the atomic and partial modes may be split
     if (splits < 1 || (splits > 1 && mode != GEMM_ATOMIC_F32 && mode != GEMM_PARTIAL_F32)) return cudaErrorInvalidValue;
     splits = gemm_tc_splits(K, splits);
@@ -492,17 +509,17 @@ cudaError_t launch_gemm_tc(const bf16_t* A, int lda, const bf16_t* W, int M, int
     if (!make_map(&mb, W, (uint64_t)w_rows, (uint64_t)K, (uint64_t)K, (uint32_t)b_box_rows(wide ? 256 : 128, mode)))
         return cudaErrorInvalidValue;
     if (wide) switch (mode) {
-        case GEMM_STORE_F32: return launch_bn<256, GEMM_STORE_F32, 4>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
-        case GEMM_ADD_F32: return launch_bn<256, GEMM_ADD_F32, 4>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
+        case GEMM_STORE_F32: return launch_bn<256, GEMM_STORE_F32, 4>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s, QkvRopeEpi{}, bias, relu);
+        case GEMM_ADD_F32: return launch_bn<256, GEMM_ADD_F32, 4>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s, QkvRopeEpi{}, bias, relu);
         case GEMM_SWIGLU_BF16: return launch_bn<256, GEMM_SWIGLU_BF16, 4>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
-        case GEMM_STORE_BF16: return launch_bn<256, GEMM_STORE_BF16, 4>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
+        case GEMM_STORE_BF16: return launch_bn<256, GEMM_STORE_BF16, 4>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s, QkvRopeEpi{}, bias, relu);
         default: return cudaErrorInvalidValue;
     }
     switch (mode) {
-        case GEMM_STORE_F32: return launch_bn<128, GEMM_STORE_F32, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
-        case GEMM_ADD_F32: return launch_bn<128, GEMM_ADD_F32, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
+        case GEMM_STORE_F32: return launch_bn<128, GEMM_STORE_F32, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s, QkvRopeEpi{}, bias, relu);
+        case GEMM_ADD_F32: return launch_bn<128, GEMM_ADD_F32, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s, QkvRopeEpi{}, bias, relu);
         case GEMM_SWIGLU_BF16: return launch_bn<128, GEMM_SWIGLU_BF16, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
-        case GEMM_STORE_BF16: return launch_bn<128, GEMM_STORE_BF16, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
+        case GEMM_STORE_BF16: return launch_bn<128, GEMM_STORE_BF16, 6>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s, QkvRopeEpi{}, bias, relu);
         // split-K CTAs run few k-blocks each: a 3-stage ring (97 KB) lets two share an SM
         case GEMM_ATOMIC_F32: return launch_bn<128, GEMM_ATOMIC_F32, 3>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);
         case GEMM_PARTIAL_F32: return launch_bn<128, GEMM_PARTIAL_F32, 3>(ma, mb, M, N, K, up_off, Cf, Cb, ldc, splits, s);

@@ -98,3 +98,26 @@ def test_gemm_tile_width_setting_without_a_gpu(lib):
     assert lib.qdec_op_gemm_tile_width(192) == -1
     assert lib.qdec_op_gemm_tile_width(0) == 128
     assert lib.qdec_op_gemm_tile_width(0) == 0
+
+
+def test_fake_token_len_through_the_abi(lib):
+    """The adaptor's row count on the host, against the oracle's definition and the page's
+    worked example (183 frames -> 23 rows)."""
+    import oracle
+    assert _lib.fake_token_len(183) == 23
+    for n in list(range(1, 70)) + [390, 1000, 3120, 4095]:
+        assert _lib.fake_token_len(n) == oracle.fake_token_len(n), n
+    assert _lib.fake_token_len(0) == 0
+
+
+def test_adaptor_create_rejects_bad_arguments_on_host(lib):
+    h = C.c_void_p()
+    w = _lib.QdecAdaptorWeights()
+    cfg = _lib.QdecAdaptorConfig(512, 2048, 1024, 8, 256, 2, 1e-12)
+    assert lib.qdec_adaptor_create(None, C.byref(w), None, C.byref(h)) == -1
+    assert lib.qdec_adaptor_create(C.byref(cfg), C.byref(w), None, C.byref(h)) == -1   # null weights
+    bad = _lib.QdecAdaptorConfig(512, 2048, 1000, 8, 256, 2, 1e-12)                     # head_dim 125
+    assert lib.qdec_adaptor_create(C.byref(bad), C.byref(w), None, C.byref(h)) == -7
+    zero = _lib.QdecAdaptorConfig(512, 2048, 1024, 8, 256, 2, 0.0)
+    assert lib.qdec_adaptor_create(C.byref(zero), C.byref(w), None, C.byref(h)) == -1
+    assert lib.qdec_adaptor_run(None, None, 1, None, None) == -1
