@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-long-prefill", action="store_true")
+    ap.add_argument("--weights", default="bf16", choices=["bf16", "q8b32", "q4b32"],
+                    help="layer weights of the decode steps (QDEC_OPT_WEIGHTS); prefill and lm_head stay bf16")
     return ap.parse_args()
 
 
@@ -151,13 +153,18 @@ def time_long_prefill(w, stream, dev, reps=7, warmup=3):
     return statistics.median(ms), ms
 
 
-def decode_step_bytes(shape, L):
+BYTES_PER_WEIGHT = {"bf16": 2.0, "q8b32": 34 / 32, "q4b32": 18 / 32}
+
+
+def decode_step_bytes(shape, L, weights="bf16"):
     """Algorithmic HBM bytes of one batch-1 decode step whose KV length after the
     append is L: every weight once (embedding row only for the gather; the full
     embedding for the tied head), the KV cache read [0, L-1), the new K/V slot
-    written, logits written."""
+    written, logits written.  `weights` is the storage of the layer matrices (codes and
+    block scales for the quantized formats); norms, embedding and lm_head stay bf16."""
     H, D, F = shape.hidden, shape.head_dim, shape.ffn
-    per_layer = (shape.qkv_rows * H + H * shape.n_q_heads * D + 2 * F * H + H * F + 2 * H + 2 * D) * 2
+    mats = shape.qkv_rows * H + H * shape.n_q_heads * D + 2 * F * H + H * F
+    per_layer = mats * BYTES_PER_WEIGHT[weights] + (2 * H + 2 * D) * 2
     weights = shape.n_layers * per_layer + shape.vocab * H * 2 + H * 2 + H * 2
     kv = (L - 1) * shape.kv_bytes_per_position + shape.kv_bytes_per_position
     return weights + kv + shape.vocab * 4
@@ -320,6 +327,10 @@ def run_ours(args):
     audio_dev = prompt.audio.to(dev)
     stream = torch.cuda.Stream(device=dev)
     dec = _lib.Decoder(shape, w, max_seq=wl.max_seq, stream=stream)
+    if args.weights != "bf16":
+        if wl.batch > 1:
+            raise SystemExit("--weights applies to the single-stream workloads")
+        dec.set_option(_lib.OPT_WEIGHTS, {"q8b32": _lib.WEIGHTS_Q8B32, "q4b32": _lib.WEIGHTS_Q4B32}[args.weights])
     if wl.batch > 1:
         return run_ours_batch(args, wl, dec, prompt, audio_dev, stream, dev, rank, world, local_rank)
 
@@ -400,7 +411,7 @@ def run_ours(args):
     # roofline of the decode step (the dominant part of the step): algorithmic bytes per
     # step averaged over the KV lengths the timed steps see, over the mean step time.
     Ls = range(wl.n_prompt + 1, wl.n_prompt + wl.n_decode + 1)
-    bytes_per_token = sum(decode_step_bytes(shape, L) for L in Ls) / len(Ls)
+    bytes_per_token = sum(decode_step_bytes(shape, L, args.weights) for L in Ls) / len(Ls)
     t_tok = dec_total_s / (wl.n_decode * args.steps)
     achieved = bytes_per_token / t_tok / 1e9
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -409,7 +420,7 @@ def run_ours(args):
             "prefill_ms": 1e3 * pre_total_s / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded random-init bf16 weights of the Qwen3-0.6B shape; seeded ids and audio rows)",
-            "config": dict(workload_desc(wl), parallelism=f"replicas{world}"),
+            "config": dict(workload_desc(wl), parallelism=f"replicas{world}", decode_weights=args.weights),
             "roofline": {"bound": "hbm",
                          "kernel": ("decode_persistent_kernel (one launch per token)" if dec.decode_kernel == 0
                                     else "decode step (graph of the CUDA-core kernels of one token)"),

@@ -191,6 +191,24 @@ int qdec_sync(const qdec_ctx *ctx);
                                         context; 0: every context attends over its own copy.
                                         Read from the batch's first context. */
 
+#define QDEC_OPT_WEIGHTS         8   /* weights of the decode steps' layer projections: */
+#define QDEC_WEIGHTS_BF16        0   /*   the borrowed bf16 matrices (default) */
+#define QDEC_WEIGHTS_Q8B32       1   /*   the library's q8b32 copy: per 32 weights along K one fp16
+                                            scale d = max|w| / 127 and int8 codes
+                                            round_half_even(w / d) (1.0625 bytes a weight) */
+#define QDEC_WEIGHTS_Q4B32       2   /*   q4b32: d = max|w| / 7, 4-bit codes (code + 8 in a nibble,
+                                            lower nibble first; 0.5625 bytes a weight)
+                                        ("Fun-ASR-Nano Native Runtime Implementation Plan", Task 8,
+                                        ships Q8_0 / Q4_K_M decoders without defining the formats;
+                                        these are the library's own).  Setting a quantized format
+                                        quantizes the layer matrices on the device into a copy the
+                                        context and its clones share, and selects
+                                        QDEC_DECODE_GRAPH (the persistent kernel reads bf16).  The
+                                        prefill, the embedding and the tied lm_head keep bf16; a
+                                        lockstep batch returns UNSUPPORTED for quantized contexts.
+                                        Needs hidden, n_q_heads * head_dim and ffn multiples of
+                                        256. */
+
 /* Sets an option.  QDEC_OPT_DECODE_KERNEL = QDEC_DECODE_PERSISTENT returns
  * UNSUPPORTED when the persistent kernel does not cover the shape (head_dim /
  * GQA group / ffn combination) or the device (cooperative launch with one

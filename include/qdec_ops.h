@@ -57,6 +57,19 @@ int qdec_op_sample(const float *logits, int32_t V, const int32_t *history, int32
                    int32_t top_k, float top_p, float repetition_penalty, uint64_t seed, int32_t pos, int32_t *token,
                    void *stream);
 
+/* Block quantization of W bf16 [N, K] (K % 32 == 0) into the library's formats
+ * (QDEC_WEIGHTS_Q8B32 / QDEC_WEIGHTS_Q4B32 of include/qdec.h; "Fun-ASR-Nano Native Runtime
+ * Implementation Plan", Task 8, names quantized decoders without defining the formats):
+ * codes int8 [N, K] (q8b32) or packed nibbles uint8 [N, K / 2] (q4b32), scales fp16
+ * [N, K / 32].  Deterministic and exact: the scale and the quotients are evaluated in double. */
+int qdec_op_quantize(const void *W, int32_t N, int32_t K, int32_t fmt, void *codes, void *scales, void *stream);
+
+/* y = W' . xhat on quantized weights (the decode GEMV): xhat = x * rsqrt(mean x^2 + eps) *
+ * norm_g when norm_g is given, else x (fp32 [K]); mode 0 stores y (fp32 [rows]), 1 adds into
+ * y, 2 stores silu(gate) * up with the up rows at row offset up_off.  K % 256 == 0. */
+int qdec_op_gemv_q(const void *codes, const void *scales, int32_t fmt, int32_t rows, int32_t K, const float *x,
+                   const void *norm_g, float eps, int32_t mode, int32_t up_off, float *y, void *stream);
+
 /* Synchronises the device and reports whether a tensor-core kernel launched
  * through these entry points gave up on a bounded wait since the last call:
  * QDEC_OK, or QDEC_E_TIMEOUT (the flag is then cleared). */

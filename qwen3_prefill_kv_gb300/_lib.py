@@ -26,6 +26,8 @@ OPT_PREFILL_IMPL = 3
 OPT_ATTN_UNIT_KEYS = 4
 OPT_SPIN_LIMIT = 5
 OPT_SHARED_PREFIX = 7
+OPT_WEIGHTS = 8
+WEIGHTS_BF16, WEIGHTS_Q8B32, WEIGHTS_Q4B32 = 0, 1, 2
 PREFILL_TCGEN05, PREFILL_SIMT = 0, 1
 DECODE_PERSISTENT, DECODE_GRAPH = 0, 1
 IMPL_SIMT, IMPL_TCGEN05 = 0, 1
@@ -84,6 +86,8 @@ SIGNATURES = [
     ("qdec_op_lm_head_scratch_bytes", _SZ, [_I32]),
     ("qdec_op_lm_head_argmax", C.c_int, [_VP, _I32, _I32, _VP, _VP, _F, _VP, _VP, _VP, _SZ, _VP]),
     ("qdec_op_lm_head_argmax_static", C.c_int, [_VP, _I32, _I32, _VP, _VP, _F, _VP, _VP, _VP]),
+    ("qdec_op_quantize", C.c_int, [_VP, _I32, _I32, _I32, _VP, _VP, _VP]),
+    ("qdec_op_gemv_q", C.c_int, [_VP, _VP, _I32, _I32, _I32, _VP, _VP, _F, _I32, _I32, _VP, _VP]),
     ("qdec_fake_token_len", C.c_int32, [_I32]),
     ("qdec_adaptor_create", C.c_int, [_VP, _VP, _VP, C.POINTER(_VP)]),
     ("qdec_adaptor_run", C.c_int, [_VP, _VP, _I32, _VP, _VP]),
@@ -301,6 +305,18 @@ def attention_prefill(Q, T, HQ, HKV, D, max_seq, pos0, k_cache, v_cache, O, impl
     lib = load()
     _check(lib.qdec_op_attention_prefill(_ptr(Q), T, HQ, HKV, D, max_seq, pos0, _ptr(k_cache), _ptr(v_cache),
                                          _ptr(O), impl, _stream_handle(stream)))
+
+
+def quantize(W, N, K, fmt, codes, scales, stream=None) -> None:
+    """qdec_op_quantize: bf16 W [N, K] -> codes (int8 [N, K] or uint8 [N, K / 2]) and fp16 scales."""
+    _check(load().qdec_op_quantize(_ptr(W), int(N), int(K), int(fmt), _ptr(codes), _ptr(scales),
+                                   _stream_handle(stream)))
+
+
+def gemv_q(codes, scales, fmt, rows, K, x, norm_g, eps, mode, y, up_off=0, stream=None) -> None:
+    """qdec_op_gemv_q: the decode GEMV on quantized weights."""
+    _check(load().qdec_op_gemv_q(_ptr(codes), _ptr(scales), int(fmt), int(rows), int(K), _ptr(x), _ptr(norm_g),
+                                 float(eps), int(mode), int(up_off), _ptr(y), _stream_handle(stream)))
 
 
 def lm_head_scratch_bytes(V: int) -> int:

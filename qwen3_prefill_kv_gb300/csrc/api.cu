@@ -53,6 +53,19 @@ struct LayerW {
     const bf16_t *wqkv, *wo, *wgu, *wd, *g_in, *g_post, *g_q, *g_k;
 };
 
+// Block-quantized copies of the layer matrices (QDEC_OPT_WEIGHTS), made once from the
+// borrowed bf16 weights and shared by a context and its clones.
+struct QuantWeights {
+    int fmt = 0;
+    std::vector<void*> bufs;   // every allocation, freed with the last user
+    struct Layer { const void *c[4], *sc[4]; };   // codes / scales of wqkv, wo, wgu, wd
+    std::vector<Layer> layers;
+    ~QuantWeights() {
+        for (void* p : bufs)
+            if (p) cudaFree(p);
+    }
+};
+
 // A stream the library created; shared by a context and its clones and destroyed with
 // the last of them.
 struct OwnedStream {
@@ -201,6 +214,7 @@ struct qdec_ctx {
     int attn_unit_keys = 0;      // QDEC_OPT_ATTN_UNIT_KEYS (0 = default)
     int spin_limit = 0;          // QDEC_OPT_SPIN_LIMIT (0 = default)
     int shared_prefix = 1;       // QDEC_OPT_SHARED_PREFIX
+    std::shared_ptr<QuantWeights> quant;   // QDEC_OPT_WEIGHTS other than bf16
     // Which prefill this context's KV prefix comes from, and how many of its positions came from
     // it: a prefill takes a new id and inherits its prompt; a clone keeps both.  Positions below
     // `inherited` are never rewritten, so contexts with one id hold the same [0, inherited).
@@ -337,6 +351,51 @@ int alloc_persistent(qdec_ctx* c) {
     CK(cudaMemset(c->am_count, 0, sizeof(unsigned int)));
     c->persistent_ok = true;
     c->decode_kernel = QDEC_DECODE_PERSISTENT;
+    return QDEC_OK;
+}
+
+// QDEC_OPT_WEIGHTS: quantizes the layer matrices on the device into a shared copy (the
+// decode step then runs its projections on it with the per-operation kernels), or drops it.
+int set_weight_format(qdec_ctx* c, int fmt) {
+    if (fmt != QDEC_WEIGHTS_BF16 && fmt != QDEC_WEIGHTS_Q8B32 && fmt != QDEC_WEIGHTS_Q4B32)
+        return fail(QDEC_E_INVALID_ARG, "QDEC_OPT_WEIGHTS takes 0 (bf16), 1 (q8b32) or 2 (q4b32)");
+    const Shape& sh = c->sh;
+    if (fmt != QDEC_WEIGHTS_BF16 && (sh.H % 256 || (sh.HQ * sh.D) % 256 || sh.F % 256))
+        return fail(QDEC_E_UNSUPPORTED, "quantized decode needs hidden, q width and ffn multiples of 256");
+    if ((c->quant ? c->quant->fmt : 0) == fmt) return QDEC_OK;
+    CK(cudaStreamSynchronize(c->stream));
+    if (c->decode_exec) {   // the captured step reads the old weights
+        cudaGraphExecDestroy(c->decode_exec);
+        c->decode_exec = nullptr;
+    }
+    if (fmt == QDEC_WEIGHTS_BF16) {
+        c->quant.reset();
+        if (c->persistent_ok) c->decode_kernel = QDEC_DECODE_PERSISTENT;
+        return QDEC_OK;
+    }
+    auto q = std::make_shared<QuantWeights>();
+    q->fmt = fmt;
+    q->layers.resize(sh.NL);
+    const int qf = fmt == QDEC_WEIGHTS_Q8B32 ? QUANT_Q8B32 : QUANT_Q4B32;
+    for (int l = 0; l < sh.NL; ++l) {
+        const LayerW& w = c->layers[l];
+        const bf16_t* mats[4] = {w.wqkv, w.wo, w.wgu, w.wd};
+        const int rows[4] = {sh.qkv_rows(), sh.H, 2 * sh.F, sh.H};
+        const int ks[4] = {sh.H, sh.HQ * sh.D, sh.H, sh.F};
+        for (int m = 0; m < 4; ++m) {
+            void *codes = nullptr, *scales = nullptr;
+            CK(cudaMalloc(&codes, quant_code_bytes(qf, rows[m], ks[m])));
+            q->bufs.push_back(codes);
+            CK(cudaMalloc(&scales, quant_scale_bytes(rows[m], ks[m])));
+            q->bufs.push_back(scales);
+            CK(launch_quantize(mats[m], rows[m], ks[m], qf, codes, scales, c->stream));
+            q->layers[l].c[m] = codes;
+            q->layers[l].sc[m] = scales;
+        }
+    }
+    CK(cudaStreamSynchronize(c->stream));
+    c->quant = q;
+    c->decode_kernel = QDEC_DECODE_GRAPH;
     return QDEC_OK;
 }
 
@@ -494,14 +553,28 @@ int enqueue_decode_body(qdec_ctx* c, cudaStream_t s) {
     const Shape& sh = c->sh;
     for (int l = 0; l < sh.NL; ++l) {
         const LayerW& w = c->layers[l];
-        CK(launch_gemv(w.wqkv, sh.qkv_rows(), sh.H, c->d_x, w.g_in, sh.eps, GEMV_STORE, 0, c->d_qkv, s));
+        const QuantWeights::Layer* ql = c->quant ? &c->quant->layers[l] : nullptr;
+        const int qf = c->quant ? c->quant->fmt : 0;
+        if (ql)
+            CK(launch_gemv_q(ql->c[0], ql->sc[0], qf, sh.qkv_rows(), sh.H, c->d_x, w.g_in, sh.eps, GEMV_STORE, 0,
+                             c->d_qkv, s));
+        else
+            CK(launch_gemv(w.wqkv, sh.qkv_rows(), sh.H, c->d_x, w.g_in, sh.eps, GEMV_STORE, 0, c->d_qkv, s));
         CK(launch_qk_norm_rope_append(c->d_qkv, 1, sh, c->d_pos, w.g_q, w.g_k, c->rope, nullptr, c->d_q,
                                       c->k_cache(l), c->v_cache(l), s));
         CK(launch_attention_decode(c->d_q, sh, c->d_pos, c->k_cache(l), c->v_cache(l), c->n_split, c->d_part_ml,
                                    c->d_part_o, c->d_attn, s));
-        CK(launch_gemv(w.wo, sh.H, sh.HQ * sh.D, c->d_attn, nullptr, sh.eps, GEMV_ADD, 0, c->d_x, s));
-        CK(launch_gemv(w.wgu, sh.F, sh.H, c->d_x, w.g_post, sh.eps, GEMV_SWIGLU, sh.F, c->d_h, s));
-        CK(launch_gemv(w.wd, sh.H, sh.F, c->d_h, nullptr, sh.eps, GEMV_ADD, 0, c->d_x, s));
+        if (ql) {
+            CK(launch_gemv_q(ql->c[1], ql->sc[1], qf, sh.H, sh.HQ * sh.D, c->d_attn, nullptr, sh.eps, GEMV_ADD, 0,
+                             c->d_x, s));
+            CK(launch_gemv_q(ql->c[2], ql->sc[2], qf, sh.F, sh.H, c->d_x, w.g_post, sh.eps, GEMV_SWIGLU, sh.F, c->d_h,
+                             s));
+            CK(launch_gemv_q(ql->c[3], ql->sc[3], qf, sh.H, sh.F, c->d_h, nullptr, sh.eps, GEMV_ADD, 0, c->d_x, s));
+        } else {
+            CK(launch_gemv(w.wo, sh.H, sh.HQ * sh.D, c->d_attn, nullptr, sh.eps, GEMV_ADD, 0, c->d_x, s));
+            CK(launch_gemv(w.wgu, sh.F, sh.H, c->d_x, w.g_post, sh.eps, GEMV_SWIGLU, sh.F, c->d_h, s));
+            CK(launch_gemv(w.wd, sh.H, sh.F, c->d_h, nullptr, sh.eps, GEMV_ADD, 0, c->d_x, s));
+        }
     }
     CK(launch_lm_head_argmax(c->embed, sh.V, sh.H, c->d_x, c->final_norm, sh.eps, c->d_logits, c->d_argmax,
                              c->d_lm_scratch, s));
@@ -1038,6 +1111,8 @@ int qdec_decode_step_batch(qdec_ctx* const* ctxs, int32_t n, const int32_t* toke
             if (ctxs[j] == ctxs[i]) return fail(QDEC_E_INVALID_ARG, "context %d repeated in the batch", i);
         if (n > 1 && ctxs[i]->sampling())
             return fail(QDEC_E_UNSUPPORTED, "the lockstep batch step is greedy: context %d samples", i);
+        if (n > 1 && ctxs[i]->quant)
+            return fail(QDEC_E_UNSUPPORTED, "the lockstep batch step reads bf16 weights: context %d is quantized", i);
     }
     if (n == 1) return qdec_decode_step(ctxs[0], tokens[0], logits_out, argmax_out);
     return batch_step(ctxs, n, tokens, logits_out, argmax_out);
@@ -1088,6 +1163,7 @@ int qdec_clone(const qdec_ctx* src, qdec_ctx** out) {
     c->attn_unit_keys = src->attn_unit_keys;
     c->spin_limit = src->spin_limit;
     c->shared_prefix = src->shared_prefix;
+    c->quant = src->quant;
     c->prefix_id = src->prefix_id;
     c->inherited = src->inherited < src->position ? src->inherited : src->position;
     c->samp_t = src->samp_t; c->samp_p = src->samp_p; c->samp_r = src->samp_r; c->samp_k = src->samp_k;
@@ -1143,6 +1219,7 @@ int qdec_set_option(qdec_ctx* c, int32_t option, int32_t value) {
         c->attn_unit_keys = value;
         return QDEC_OK;
     }
+    if (option == QDEC_OPT_WEIGHTS) return set_weight_format(c, value);
     if (option == QDEC_OPT_SHARED_PREFIX) {
         if (value != 0 && value != 1) return fail(QDEC_E_INVALID_ARG, "QDEC_OPT_SHARED_PREFIX takes 0 or 1");
         c->shared_prefix = value;
@@ -1172,6 +1249,8 @@ int qdec_set_option(qdec_ctx* c, int32_t option, int32_t value) {
         return fail(QDEC_E_INVALID_ARG, "bad value %d for QDEC_OPT_DECODE_KERNEL", value);
     if (value == QDEC_DECODE_PERSISTENT && !c->persistent_ok)
         return fail(QDEC_E_UNSUPPORTED, "the persistent decode kernel does not cover this shape or device");
+    if (value == QDEC_DECODE_PERSISTENT && c->quant)
+        return fail(QDEC_E_UNSUPPORTED, "quantized weights decode with the per-operation kernels");
     c->decode_kernel = value;
     return QDEC_OK;
 }
@@ -1197,6 +1276,7 @@ int qdec_get_option(const qdec_ctx* c, int32_t option) {
     if (option == QDEC_OPT_ATTN_UNIT_KEYS) return c->attn_unit_keys;
     if (option == QDEC_OPT_SPIN_LIMIT) return c->spin_limit;
     if (option == QDEC_OPT_SHARED_PREFIX) return c->shared_prefix;
+    if (option == QDEC_OPT_WEIGHTS) return c->quant ? c->quant->fmt : QDEC_WEIGHTS_BF16;
     if (option != QDEC_OPT_DECODE_KERNEL) return fail(QDEC_E_INVALID_ARG, "unknown option %d", option);
     return c->decode_kernel;
 }

@@ -158,6 +158,16 @@ enum GemvMode { GEMV_STORE = 0, GEMV_ADD = 1, GEMV_SWIGLU = 2 };
 cudaError_t launch_gemv(const bf16_t* W, int rows, int K, const float* x, const bf16_t* norm_g,
                         float eps, int mode, int up_off, float* y, cudaStream_t s);
 
+// Block-quantized layer weights (k_quant.cu): QUANT_Q8B32 int8 codes [N, K], QUANT_Q4B32
+// nibbles [N, K / 2] (lower nibble first, code + 8); fp16 scales [N, K / 32] for both.
+enum QuantFormat { QUANT_NONE = 0, QUANT_Q8B32 = 1, QUANT_Q4B32 = 2 };
+size_t quant_code_bytes(int fmt, size_t N, size_t K);
+size_t quant_scale_bytes(size_t N, size_t K);
+cudaError_t launch_quantize(const bf16_t* W, int N, int K, int fmt, void* codes, void* scales, cudaStream_t s);
+// launch_gemv on quantized weights (K a multiple of 256).
+cudaError_t launch_gemv_q(const void* codes, const void* scales, int fmt, int rows, int K, const float* x,
+                          const bf16_t* norm_g, float eps, int mode, int up_off, float* y, cudaStream_t s);
+
 // Tied lm_head on one row with fused final RMSNorm and a deterministic grid argmax.
 // scratch: >= lm_head_scratch_bytes(V); its first 4 bytes (ticket counter) must be zero
 // before the first launch and are returned to zero by every launch.

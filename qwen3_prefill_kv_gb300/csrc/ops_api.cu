@@ -65,6 +65,25 @@ int qdec_op_sample(const float* logits, int32_t V, const int32_t* history, int32
                                      (unsigned long long)seed, pos, token, static_cast<cudaStream_t>(stream)));
 }
 
+int qdec_op_quantize(const void* W, int32_t N, int32_t K, int32_t fmt, void* codes, void* scales, void* stream) {
+    if (!W || !codes || !scales || N <= 0 || K <= 0 || K % 32 != 0 || (fmt != 1 && fmt != 2))
+        return set_error(QDEC_E_INVALID_ARG, "qdec_op_quantize: null pointer, bad size or format");
+    cudaError_t e = launch_quantize(static_cast<const bf16_t*>(W), N, K, fmt == 1 ? QUANT_Q8B32 : QUANT_Q4B32, codes,
+                                    scales, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QDEC_OK : set_error(QDEC_E_CUDA, "qdec_op_quantize: %s", cudaGetErrorString(e));
+}
+
+int qdec_op_gemv_q(const void* codes, const void* scales, int32_t fmt, int32_t rows, int32_t K, const float* x,
+                   const void* norm_g, float eps, int32_t mode, int32_t up_off, float* y, void* stream) {
+    if (!codes || !scales || !x || !y || rows <= 0 || K <= 0 || K % 256 != 0 || (fmt != 1 && fmt != 2) || mode < 0 ||
+        mode > 2)
+        return set_error(QDEC_E_INVALID_ARG, "qdec_op_gemv_q: null pointer, bad size, format or mode");
+    cudaError_t e = launch_gemv_q(codes, scales, fmt == 1 ? QUANT_Q8B32 : QUANT_Q4B32, rows, K, x,
+                                  static_cast<const bf16_t*>(norm_g), eps, mode, up_off, y,
+                                  static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? QDEC_OK : set_error(QDEC_E_CUDA, "qdec_op_gemv_q: %s", cudaGetErrorString(e));
+}
+
 int qdec_op_device_error(void) {
     const int v1 = tc_error_read_and_clear(), v2 = fa_error_read_and_clear();
     if (v1 < 0 || v2 < 0) return set_error(QDEC_E_CUDA, "reading the device error word failed");
