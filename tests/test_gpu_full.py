@@ -117,6 +117,30 @@ def test_persistent_and_graph_decode_agree(full):
             assert np.abs(ka - kb).max() <= 2e-2 * np.abs(kb).max()
 
 
+def test_mid_length_prefill(full):
+    """A 1100-position prompt (30 ids, 1040 audio rows, 30 ids): every projection has enough
+    tiles to run unsplit on 128 x 256 tiles, and attention spans nine 128-key tiles.  Logits
+    of the prefill and two decode steps against the oracle; KV slots of the first, middle and
+    last layer against the CUDA-core prefill: each path is within 1e-2 of max|ref| of the exact
+    slots (one bf16 rounding per operand over the layers), so the two agree to the sum, 2e-2."""
+    w, wd, orc = full
+    wl = synth.Workload("mid", SH, 30, 1040, 30, 2)
+    p = synth.make_prompt(wl, seed=3)
+    dec = Decoder(SH, wd, max_seq=wl.max_seq)
+    res = H.teacher_forced(dec, orc.clone(), p, 2)
+    H.assert_step_parity(res, "1100 positions")
+    _report("prefill_1100", res)
+    ref = Decoder(SH, wd, max_seq=wl.n_prompt)
+    ref.set_option(_lib.OPT_PREFILL_IMPL, _lib.PREFILL_SIMT)
+    ref.prefill(p.ids, p.audio.cuda(), p.audio_offset)
+    f = lambda u: (u.astype(np.uint32) << 16).view(np.float32)
+    for layer in (0, 13, SH.n_layers - 1):
+        for kind in (0, 1):
+            a = f(dec.read_kv(layer, kind, 0, wl.n_prompt))
+            b = f(ref.read_kv(layer, kind, 0, wl.n_prompt))
+            np.testing.assert_allclose(a, b, rtol=0, atol=2e-2 * float(np.abs(b).max()), err_msg=f"{layer} {kind}")
+
+
 @pytest.mark.slow
 def test_long_context_prefill_and_steps(full):
     w, wd, orc = full
