@@ -50,6 +50,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-long-prefill", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="streams of the branching workload (default: the workload's 64); for small profiling runs")
+    ap.add_argument("--long-prefill-only", action="store_true",
+                    help="time only the 4096-position prefill and print its roofline (a profiling target)")
     ap.add_argument("--weights", default="bf16", choices=["bf16", "q8b32", "q4b32"],
                     help="layer weights of the decode steps (QDEC_OPT_WEIGHTS); prefill and lm_head stay bf16")
     return ap.parse_args()
@@ -319,9 +323,21 @@ def run_ours(args):
     build.build()
     _lib.load()
     wl = synth.WORKLOADS[args.workload]
+    if args.batch and wl.batch > 1:
+        import dataclasses
+        wl = dataclasses.replace(wl, batch=args.batch)
     shape = wl.shape
     dev = torch.device("cuda", local_rank)
     w = synth.make_weights(shape, seed=0).to(dev)
+    if args.long_prefill_only:
+        stream = torch.cuda.Stream(device=dev)
+        med, all_ms = time_long_prefill(w, stream, dev)
+        _, bf16, peak_kind = peaks()
+        fl = prefill_flops(shape, 4096)
+        if rank == 0:
+            print(json.dumps({"prefill_4096_ms": med, "ms_all": all_ms, "tflops": fl / (med * 1e-3) / 1e12,
+                              "frac": fl / (med * 1e-3) / 1e12 / bf16, "peak_kind": peak_kind}), flush=True)
+        return
     prompt = synth.make_prompt(wl, seed=rank)
     ids = prompt.ids
     audio_dev = prompt.audio.to(dev)

@@ -8,7 +8,7 @@
 // w' = q * d, an all-zero block has d = 0 and codes 0.  The quantizer computes the scale
 // and the quotients in double (the same roundings as the definition), so its codes and
 // scales are exact.  The decode GEMV streams the codes and scales and dequantizes in
-// registers: every product is q * x in fp32, and a lane's 8 columns share one block scale.
+// registers: every product is q * x in fp32, and a lane's 16 columns share one block scale.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -65,28 +65,35 @@ __global__ void quantize_kernel(const bf16_t* __restrict__ W, int N, int K, int 
     }
 }
 
-constexpr int GQ_THREADS = 256;
+constexpr int GQ_THREADS = 128;   // 4 warps, each R rows: many small CTAs keep every SM streaming
+constexpr int GQ_R = 2;
+constexpr int GQ_MAXC = 6;         // 16-code chunks a lane loads per row (K <= 32 * 16 * 6 = 3072)
 
-// 8 codes of one row (columns k .. k + 7, one block) times x, unscaled.
+// 16 codes of one row (columns k .. k + 15, half a block) times x, unscaled.
 template <int BITS>
-__device__ __forceinline__ float qdot8(const void* row_codes, int k, const float* xv) {
+__device__ __forceinline__ float qdot16(const uint4 c, const float* xv) {
     float a = 0.f;
     if constexpr (BITS == 8) {
-        const uint2 c = __ldcs(reinterpret_cast<const uint2*>(static_cast<const int8_t*>(row_codes) + k));
+        const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) a = fmaf((float)(int8_t)(c.x >> (8 * j)), xv[j], a);
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) a = fmaf((float)(int8_t)(c.y >> (8 * j)), xv[4 + j], a);
-    } else {
-        const uint32_t c = __ldcs(reinterpret_cast<const unsigned int*>(static_cast<const uint8_t*>(row_codes) + k / 2));
+            for (int j = 0; j < 4; ++j) a = fmaf((float)(int8_t)(w[i] >> (8 * j)), xv[4 * i + j], a);
+    } else {   // 16 nibbles in the low 8 bytes (c.x, c.y)
+        const uint32_t w[2] = {c.x, c.y};
 #pragma unroll
-        for (int j = 0; j < 8; ++j) a = fmaf((float)((int)((c >> (4 * j)) & 15u) - 8), xv[j], a);
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) a = fmaf((float)((int)((w[i] >> (4 * j)) & 15u) - 8), xv[8 * i + j], a);
     }
     return a;
 }
 
-// y = W' . xhat for quantized W' (each warp R consecutive rows; SWIGLU: the up rows at up_off).
-template <int MODE, int R, int BITS>
+// y = W' . xhat for quantized W'.  Each warp owns GQ_R consecutive rows (SWIGLU: and the up
+// rows at up_off); lane l takes the 16-column chunks l, l + 32, ... of every row.  All of a
+// lane's code and scale loads are issued before any arithmetic (up to GQ_MAXC chunks per
+// row in flight), which is what keeps HBM busy for a small matrix.
+template <int MODE, int BITS>
 __global__ void __launch_bounds__(GQ_THREADS) gemv_q_kernel(const void* __restrict__ codes,
                                                            const __half* __restrict__ scales, int rows, int K,
                                                            const float* __restrict__ x,
@@ -94,6 +101,36 @@ __global__ void __launch_bounds__(GQ_THREADS) gemv_q_kernel(const void* __restri
                                                            float* __restrict__ y) {
     extern __shared__ float xs[];
     __shared__ float red[GQ_THREADS / 32];
+    constexpr int NA = (MODE == GEMV_SWIGLU) ? 2 : 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row0 = (blockIdx.x * (GQ_THREADS / 32) + warp) * GQ_R;
+    const int nchunk = K / 16, nc = (nchunk - lane + 31) / 32;   // chunks of this lane per row
+    const size_t row_bytes = BITS == 8 ? (size_t)K : (size_t)K / 2;
+    const int nb = K / 32;
+    // issue the weight loads first: they do not depend on x
+    uint4 cw[NA][GQ_R][GQ_MAXC];
+    float sc[NA][GQ_R][GQ_MAXC];
+#pragma unroll
+    for (int a = 0; a < NA; ++a)
+#pragma unroll
+        for (int r = 0; r < GQ_R; ++r) {
+            const int row = min(row0 + r, rows - 1);
+            const size_t rr = (size_t)(row + a * up_off);
+            const uint8_t* cb = static_cast<const uint8_t*>(codes) + rr * row_bytes;
+#pragma unroll
+            for (int i = 0; i < GQ_MAXC; ++i) {
+                if (i < nc) {
+                    const int ch = lane + 32 * i;
+                    if (BITS == 8) {
+                        cw[a][r][i] = __ldcs(reinterpret_cast<const uint4*>(cb + (size_t)ch * 16));
+                    } else {
+                        const uint2 v = __ldcs(reinterpret_cast<const uint2*>(cb + (size_t)ch * 8));
+                        cw[a][r][i] = make_uint4(v.x, v.y, 0u, 0u);
+                    }
+                    sc[a][r][i] = __half2float(scales[rr * nb + (ch >> 1)]);
+                }
+            }
+        }
     float ss = 0.f;
     for (int i = threadIdx.x * 4; i < K; i += GQ_THREADS * 4) {
         const float4 v = *reinterpret_cast<const float4*>(x + i);
@@ -102,7 +139,7 @@ __global__ void __launch_bounds__(GQ_THREADS) gemv_q_kernel(const void* __restri
     }
     if (norm_g) {
         ss = warp_sum(ss);
-        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+        if (lane == 0) red[warp] = ss;
         __syncthreads();
         float tot = 0.f;
 #pragma unroll
@@ -111,35 +148,26 @@ __global__ void __launch_bounds__(GQ_THREADS) gemv_q_kernel(const void* __restri
         for (int i = threadIdx.x; i < K; i += GQ_THREADS) xs[i] = xs[i] * r * bf1(norm_g[i]);
     }
     __syncthreads();
-    constexpr int NA = (MODE == GEMV_SWIGLU) ? 2 : 1;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row0 = (blockIdx.x * (GQ_THREADS / 32) + warp) * R;
-    const size_t row_bytes = BITS == 8 ? (size_t)K : (size_t)K / 2;
-    const int nb = K / 32;
-    float acc[NA][R];
+    float acc[NA][GQ_R];
 #pragma unroll
     for (int a = 0; a < NA; ++a)
 #pragma unroll
-        for (int r = 0; r < R; ++r) acc[a][r] = 0.f;
-    for (int k = lane * 8; k < K; k += 256) {
-        float xv[8];
-        *reinterpret_cast<float4*>(xv) = *reinterpret_cast<const float4*>(xs + k);
-        *reinterpret_cast<float4*>(xv + 4) = *reinterpret_cast<const float4*>(xs + k + 4);
+        for (int r = 0; r < GQ_R; ++r) acc[a][r] = 0.f;
 #pragma unroll
-        for (int a = 0; a < NA; ++a)
+    for (int i = 0; i < GQ_MAXC; ++i) {
+        if (i < nc) {
+            float xv[16];
+            const float4* xp = reinterpret_cast<const float4*>(xs + (lane + 32 * i) * 16);
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const int row = row0 + r;
-                if (row < rows) {
-                    const size_t rr = (size_t)(row + a * up_off);
-                    const float d = __half2float(scales[rr * nb + (k >> 5)]);
-                    acc[a][r] = fmaf(d, qdot8<BITS>(static_cast<const uint8_t*>(codes) + rr * row_bytes, k, xv),
-                                     acc[a][r]);
-                }
-            }
+            for (int j = 0; j < 4; ++j) *reinterpret_cast<float4*>(xv + 4 * j) = xp[j];
+#pragma unroll
+            for (int a = 0; a < NA; ++a)
+#pragma unroll
+                for (int r = 0; r < GQ_R; ++r) acc[a][r] = fmaf(sc[a][r][i], qdot16<BITS>(cw[a][r][i], xv), acc[a][r]);
+        }
     }
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
+    for (int r = 0; r < GQ_R; ++r) {
         const int row = row0 + r;
         const float v0 = warp_sum(acc[0][r]);
         const float v1 = NA > 1 ? warp_sum(acc[NA - 1][r]) : 0.f;
@@ -154,18 +182,17 @@ __global__ void __launch_bounds__(GQ_THREADS) gemv_q_kernel(const void* __restri
 template <int BITS>
 cudaError_t launch_gemv_q_bits(const void* codes, const __half* scales, int rows, int K, const float* x,
                                const bf16_t* norm_g, float eps, int mode, int up_off, float* y, cudaStream_t s) {
-    constexpr int R = 2;
-    const int grid = (rows + (GQ_THREADS / 32) * R - 1) / ((GQ_THREADS / 32) * R);
+    const int grid = (rows + (GQ_THREADS / 32) * GQ_R - 1) / ((GQ_THREADS / 32) * GQ_R);
     const size_t smem = (size_t)K * sizeof(float);
     switch (mode) {
         case GEMV_STORE:
-            gemv_q_kernel<GEMV_STORE, R, BITS><<<grid, GQ_THREADS, smem, s>>>(codes, scales, rows, K, x, norm_g, eps, up_off, y);
+            gemv_q_kernel<GEMV_STORE, BITS><<<grid, GQ_THREADS, smem, s>>>(codes, scales, rows, K, x, norm_g, eps, up_off, y);
             break;
         case GEMV_ADD:
-            gemv_q_kernel<GEMV_ADD, R, BITS><<<grid, GQ_THREADS, smem, s>>>(codes, scales, rows, K, x, norm_g, eps, up_off, y);
+            gemv_q_kernel<GEMV_ADD, BITS><<<grid, GQ_THREADS, smem, s>>>(codes, scales, rows, K, x, norm_g, eps, up_off, y);
             break;
         case GEMV_SWIGLU:
-            gemv_q_kernel<GEMV_SWIGLU, R, BITS><<<grid, GQ_THREADS, smem, s>>>(codes, scales, rows, K, x, norm_g, eps, up_off, y);
+            gemv_q_kernel<GEMV_SWIGLU, BITS><<<grid, GQ_THREADS, smem, s>>>(codes, scales, rows, K, x, norm_g, eps, up_off, y);
             break;
         default: return cudaErrorInvalidValue;
     }
@@ -193,7 +220,7 @@ cudaError_t launch_quantize(const bf16_t* W, int N, int K, int fmt, void* codes,
 cudaError_t launch_gemv_q(const void* codes, const void* scales, int fmt, int rows, int K, const float* x,
                           const bf16_t* norm_g, float eps, int mode, int up_off, float* y, cudaStream_t s) {
     (void)cudaGetLastError();
-    if (K % 256 != 0) return cudaErrorInvalidValue;   // a lane's 8 columns per 256-column chunk
+    if (K % 256 != 0 || K > 32 * 16 * GQ_MAXC) return cudaErrorInvalidValue;   // whole 16-column chunks per lane
     const __half* sc = static_cast<const __half*>(scales);
     if (fmt == QUANT_Q8B32) return launch_gemv_q_bits<8>(codes, sc, rows, K, x, norm_g, eps, mode, up_off, y, s);
     if (fmt == QUANT_Q4B32) return launch_gemv_q_bits<4>(codes, sc, rows, K, x, norm_g, eps, mode, up_off, y, s);
