@@ -28,7 +28,9 @@ extern "C" {
  * (row-major, K contiguous), fp32 accumulation, and the epilogue `mode`
  * ("Forward map - funasr_nano", LLM decoder table: the block's projections,
  * residual adds and packed gate_up SwiGLU).  ldc is C's row stride in
- * elements.  Shape limits: K % 64 == 0 for TCGEN05, K % 32 == 0 for SIMT. */
+ * elements.  Shape limits: K % 64 == 0 for TCGEN05, K % 32 == 0 for SIMT;
+ * TCGEN05 also needs C 16-byte aligned with ldc >= N and ldc x element size a
+ * multiple of 16 bytes (its epilogue writes C by TMA). */
 int qdec_op_gemm(const void *A, int32_t lda, const void *W, int32_t M, int32_t N, int32_t K, int32_t mode,
                  int32_t up_off, void *C, int32_t ldc, int32_t impl, void *stream);
 
@@ -47,6 +49,14 @@ int qdec_op_gemm_splitk(const void *A, int32_t lda, const void *W, int32_t M, in
  * and not thread-safe: meant for tuning and tests.  Returns the previous
  * setting, or QDEC_E_INVALID_ARG for any other value. */
 int qdec_op_gemm_tile_width(int32_t bn);
+
+/* Tile height of the 256-wide tcgen05 GEMM tiles: 128 runs each tile on one CTA, 256 runs
+ * 256 x 256 tiles on a pair of CTAs (a cluster of two SMs, tcgen05 cta_group::2, each CTA
+ * loading its own 128 rows of A and of B), 0 (the default) lets the library choose, which
+ * is one CTA: the pair measured slower on every prefill shape.
+ * Process-wide and not thread-safe: for tuning and tests.  Returns the previous setting, or
+ * QDEC_E_INVALID_ARG for any other value. */
+int qdec_op_gemm_tile_rows(int32_t bm);
 
 /* The token choice of qdec_set_sampling (include/qdec.h) on one logits vector: logits
  * fp32 [V] (device), history int32 [n_history] (device ids; ids outside [0, V) are

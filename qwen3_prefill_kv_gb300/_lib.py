@@ -79,6 +79,7 @@ SIGNATURES = [
     ("qdec_op_gemm", C.c_int, [_VP, _I32, _VP, _I32, _I32, _I32, _I32, _I32, _VP, _I32, _I32, _VP]),
     ("qdec_op_device_error", C.c_int, []),
     ("qdec_op_gemm_tile_width", C.c_int, [C.c_int32]),
+    ("qdec_op_gemm_tile_rows", C.c_int, [C.c_int32]),
     ("qdec_op_sample", C.c_int, [_VP, _I32, _VP, _I32, _F, _I32, _F, _F, C.c_uint64, _I32, _VP, _VP]),
     ("qdec_set_sampling", C.c_int, [_VP, _F, _I32, _F, _F, C.c_uint64]),
     ("qdec_op_gemm_splitk", C.c_int, [_VP, _I32, _VP, _I32, _I32, _I32, _I32, _VP, _I32, _VP]),
@@ -294,6 +295,14 @@ def sample(logits, V, history, temperature, top_k, top_p, repetition_penalty, se
     _check(load().qdec_op_sample(_ptr(logits), int(V), _ptr(history) if n else None, n, float(temperature),
                                  int(top_k), float(top_p), float(repetition_penalty), int(seed) & ((1 << 64) - 1),
                                  int(pos), _ptr(token_out), _stream_handle(stream)))
+
+
+def gemm_tile_rows(bm: int) -> int:
+    """Forces the height of the 256-wide tcgen05 GEMM tiles (128: one CTA, 256: a CTA pair;
+    0 = per shape); returns the previous setting."""
+    rc = int(load().qdec_op_gemm_tile_rows(int(bm)))
+    _check(min(rc, 0))
+    return rc
 
 
 def device_error() -> None:

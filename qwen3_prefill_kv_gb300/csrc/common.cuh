@@ -99,6 +99,9 @@ int gemm_tc_splits(int K, int splits);
 // setting.  Process-wide, not thread-safe: for tuning and tests.
 int set_gemm_tile_width(int bn);
 int gemm_tile_width();   // the current setting (0, 128 or 256)
+// The same for the tile height of the 256-wide tiles (128 or 256 rows; 0 = chosen per shape).
+int set_gemm_tile_rows(int bm);
+int gemm_tile_rows();
 // bias (fp32 [N], optional) is added to every row and relu (0/1) clamps at zero, after the
 // accumulation, in the STORE_F32, ADD_F32 (C += acc + bias) and STORE_BF16 modes.
 cudaError_t launch_gemm_tc(const bf16_t* A, int lda, const bf16_t* W, int M, int N, int K, int mode, int up_off,

@@ -31,6 +31,8 @@ int qdec_op_gemm(const void* A, int32_t lda, const void* W, int32_t M, int32_t N
     if (impl == QDEC_IMPL_TCGEN05) {
         if (!gemm_tc_supported(N, K, mode, lda))
             return set_error(QDEC_E_UNSUPPORTED, "tcgen05 GEMM needs K %% 64 == 0, N %% 128 == 0 (SwiGLU: %% 64)");
+        if (reinterpret_cast<uintptr_t>(C) % 16 != 0 || ((size_t)ldc * (f32 ? 4 : 2)) % 16 != 0 || ldc < N)
+            return set_error(QDEC_E_UNSUPPORTED, "tcgen05 GEMM needs C 16-byte aligned, ldc >= N, rows 16-byte multiples");
         return cuda_status(launch_gemm_tc(static_cast<const bf16_t*>(A), lda, static_cast<const bf16_t*>(W), M, N, K,
                                           mode, up_off, Cf, Cb, ldc, s));
     }
@@ -45,6 +47,12 @@ int qdec_op_gemm_splitk(const void* A, int32_t lda, const void* W, int32_t M, in
         return set_error(QDEC_E_UNSUPPORTED, "tcgen05 GEMM needs K %% 64 == 0, N %% 128 == 0");
     return cuda_status(launch_gemm_tc(static_cast<const bf16_t*>(A), lda, static_cast<const bf16_t*>(W), M, N, K,
                                       GEMM_ATOMIC_F32, 0, C, nullptr, ldc, static_cast<cudaStream_t>(stream), splits));
+}
+
+int qdec_op_gemm_tile_rows(int32_t bm) {
+    if (bm != 0 && bm != 128 && bm != 256)
+        return set_error(QDEC_E_INVALID_ARG, "qdec_op_gemm_tile_rows: %d is not 0, 128 or 256", bm);
+    return set_gemm_tile_rows(bm);
 }
 
 int qdec_op_gemm_tile_width(int32_t bn) {

@@ -58,12 +58,14 @@ def test_teacher_forced_workload(full, name):
     assert np.array_equal(hist[:wl.n_prompt][mask], kv_prompt[mask])
 
 
-@pytest.mark.parametrize("name,tile", [("funasr_nano_short", 0), ("qwen3_asr_30s", 0), ("qwen3_asr_30s", 256)])
+@pytest.mark.parametrize("name,tile", [("funasr_nano_short", 0), ("qwen3_asr_30s", 0), ("qwen3_asr_30s", 256),
+                                       ("qwen3_asr_30s", 256256)])
 def test_fused_qkv_epilogue_matches_separate_kernels(full, name, tile):
     """The tcgen05 prefill writes K and V from the QKV GEMM's epilogue (per-head norm + RoPE
     fused); the CUDA-core prefill runs the GEMM and the norm/RoPE/append kernel separately.
     Both caches and the prefill logits must agree to bf16 rounding.  tile=256 forces the
-    128 x 256 GEMM tiles (two heads per tile) that long prompts use."""
+    128 x 256 GEMM tiles (two heads per tile) that long prompts use, 256256 the 256 x 256
+    tiles on a CTA pair of the longest prompts."""
     w, wd, orc = full
     wl = synth.WORKLOADS[name]
     p = synth.make_prompt(wl, seed=0)
@@ -72,12 +74,14 @@ def test_fused_qkv_epilogue_matches_separate_kernels(full, name, tile):
         d = Decoder(SH, wd, max_seq=wl.n_prompt + 1)
         d.set_option(_lib.OPT_PREFILL_IMPL, impl)
         lg = torch.empty(SH.vocab, device="cuda")
-        prev = _lib.gemm_tile_width(tile)
+        prev = _lib.gemm_tile_width(tile % 1000)
+        prev_rows = _lib.gemm_tile_rows(tile // 1000)
         try:
             d.prefill(p.ids, p.audio.cuda(), p.audio_offset, logits=lg)
             d.sync()
         finally:
             _lib.gemm_tile_width(prev)
+            _lib.gemm_tile_rows(prev_rows)
         decs.append(d)
         logits.append(lg.cpu().numpy())
     for layer in (0, 13, SH.n_layers - 1):

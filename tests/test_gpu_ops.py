@@ -54,10 +54,14 @@ def test_gemm_epilogues(impl, M, N, K, mode):
 WIDE_CASES = [(1, 256, 128), (130, 512, 384), (77, 4096, 1024), (300, 1024, 2048), (415, 1024, 3072)]
 
 
+@pytest.mark.parametrize("tile_rows", [128, 256], ids=["128x256", "256x256"])
 @pytest.mark.parametrize("M,N,K", WIDE_CASES)
 @pytest.mark.parametrize("mode", [_lib.GEMM_STORE_F32, _lib.GEMM_ADD_F32, _lib.GEMM_SWIGLU_BF16, _lib.GEMM_STORE_BF16])
-def test_gemm_wide_tiles(M, N, K, mode):
-    """The tcgen05 GEMM with 128 x 256 tiles (SwiGLU: 128 gate + 128 up columns), forced."""
+def test_gemm_wide_tiles(M, N, K, mode, tile_rows):
+    """The tcgen05 GEMM with 256-wide tiles (SwiGLU: 128 gate + 128 up columns), forced, on
+    one CTA (128 rows) and on a CTA pair (256 rows, cta_group::2: each CTA loads its own 128
+    rows of A and of B; M = 1, 77, 130 and 300 leave the second CTA's rows partly or wholly
+    past the end)."""
     up_off = N + 128 if mode == _lib.GEMM_SWIGLU_BF16 else 0
     rows = up_off + N if mode == _lib.GEMM_SWIGLU_BF16 else N
     A = _bf16((M, K), 21, 0.5)
@@ -66,11 +70,13 @@ def test_gemm_wide_tiles(M, N, K, mode):
     C0 = torch.zeros(M, N) if bf else _bf16((M, N), 23).float()
     Cd = C0.to(torch.bfloat16).cuda() if bf else C0.cuda()
     prev = _lib.gemm_tile_width(256)
+    prev_rows = _lib.gemm_tile_rows(tile_rows)
     try:
         _lib.gemm(A.cuda(), W.cuda(), M, N, K, mode, Cd, up_off=up_off, impl=_lib.IMPL_TCGEN05)
         torch.cuda.synchronize()
     finally:
         _lib.gemm_tile_width(prev)
+        _lib.gemm_tile_rows(prev_rows)
     _lib.device_error()
     ref = _gemm_ref(A, W, mode, N, up_off)
     if mode == _lib.GEMM_ADD_F32:
@@ -84,6 +90,9 @@ def test_gemm_tile_width_rejects_other_values():
     with pytest.raises(_lib.QdecError):
         _lib.gemm_tile_width(192)
     assert _lib.gemm_tile_width(0) == 0
+    with pytest.raises(_lib.QdecError):
+        _lib.gemm_tile_rows(64)
+    assert _lib.gemm_tile_rows(0) == 0
 
 
 @pytest.mark.parametrize("M,N,K,splits", [(64, 4096, 1024, 8), (64, 1024, 3072, 32), (5, 256, 128, 2),
