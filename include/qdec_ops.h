@@ -58,6 +58,15 @@ int qdec_op_gemm_tile_width(int32_t bn);
  * QDEC_E_INVALID_ARG for any other value. */
 int qdec_op_gemm_tile_rows(int32_t bm);
 
+/* Programmatic dependent launch of the prefill chain (the GEMMs, attention, norms and
+ * the other kernels between the embedding and the head): 1 (the default) launches each
+ * with programmatic stream serialisation, so its CTAs start their prologue and request
+ * their first weight tiles while the preceding kernel finishes, and wait for that kernel
+ * before touching what it writes; 0 launches them plainly.  Results are identical either
+ * way.  Process-wide and not thread-safe: for measurements and tests.  Returns the previous
+ * setting, or QDEC_E_INVALID_ARG for a value other than 0 or 1. */
+int qdec_op_programmatic_launch(int32_t on);
+
 /* The token choice of qdec_set_sampling (include/qdec.h) on one logits vector: logits
  * fp32 [V] (device), history int32 [n_history] (device ids; ids outside [0, V) are
  * ignored), the draw at position `pos` under `seed`; *token (device int32) receives the

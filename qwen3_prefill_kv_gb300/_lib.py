@@ -80,6 +80,7 @@ SIGNATURES = [
     ("qdec_op_device_error", C.c_int, []),
     ("qdec_op_gemm_tile_width", C.c_int, [C.c_int32]),
     ("qdec_op_gemm_tile_rows", C.c_int, [C.c_int32]),
+    ("qdec_op_programmatic_launch", C.c_int, [C.c_int32]),
     ("qdec_op_sample", C.c_int, [_VP, _I32, _VP, _I32, _F, _I32, _F, _F, C.c_uint64, _I32, _VP, _VP]),
     ("qdec_set_sampling", C.c_int, [_VP, _F, _I32, _F, _F, C.c_uint64]),
     ("qdec_op_gemm_splitk", C.c_int, [_VP, _I32, _VP, _I32, _I32, _I32, _I32, _VP, _I32, _VP]),
@@ -301,6 +302,14 @@ def gemm_tile_rows(bm: int) -> int:
     """Forces the height of the 256-wide tcgen05 GEMM tiles (128: one CTA, 256: a CTA pair;
     0 = per shape); returns the previous setting."""
     rc = int(load().qdec_op_gemm_tile_rows(int(bm)))
+    _check(min(rc, 0))
+    return rc
+
+
+def programmatic_launch(on: int) -> int:
+    """Switches programmatic dependent launch of the prefill chain (1 = on, the default);
+    returns the previous setting."""
+    rc = int(load().qdec_op_programmatic_launch(int(on)))
     _check(min(rc, 0))
     return rc
 

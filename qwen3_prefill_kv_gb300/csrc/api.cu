@@ -983,7 +983,8 @@ int prefill_body(qdec_ctx* c, int T, cudaStream_t s, uint64_t* kernels) {
 // implementation, tile width) key is seen, from a CUDA graph captured on the second and
 // replayed after that (about 250 launches for a short prompt become one).
 int prefill_run_body(qdec_ctx* c, int T, uint64_t* kernels) {
-    const int tile = gemm_tile_width() + 1000 * gemm_tile_rows();   // both forced tile settings key the graph
+    // the forced tile settings and the launch attribute key the graph
+    const int tile = gemm_tile_width() + 1000 * gemm_tile_rows() + 1000000 * (programmatic_launch() ? 1 : 0);
     qdec_ctx::PrefillGraph* g = nullptr;
     for (auto& e : c->pf_graphs)
         if (e.T == T && e.impl == c->prefill_gemm && e.tile == tile) g = &e;

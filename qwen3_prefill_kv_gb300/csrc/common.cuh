@@ -28,6 +28,35 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
+// ---- programmatic dependent launch.  The kernels of the prefill chain call pdl_trigger() on
+// entry, which lets the stream's next kernel place its CTAs (prologue, weight prefetch)
+// while this grid finishes, and pdl_wait() before their first access to anything an earlier
+// kernel of the stream writes: it returns once the preceding grid has completed and its
+// writes are visible (at once for a kernel launched without the attribute).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Process-wide switch of the launch attribute (on unless switched off); returns the previous value.
+int set_programmatic_launch(int on);
+bool programmatic_launch();
+
+// kern<<<grid, block, smem, s>>>(args...) with programmatic stream serialisation when the
+// switch is on (the kernel must then call pdl_wait() as described above).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = programmatic_launch() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // silu(z) = z / (1 + e^-z)
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 

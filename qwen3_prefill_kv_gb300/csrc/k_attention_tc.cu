@@ -131,6 +131,7 @@ __global__ void __launch_bounds__(192, 1) attn_prefill_tc_kernel(const __grid_co
                                                                  const __grid_constant__ CUtensorMap tmV, int T,
                                                                  int HQ, int HKV, int pos0, bf16_t* __restrict__ O,
                                                                  float scale_log2, int causal) {
+    pdl_trigger();
     extern __shared__ __align__(1024) char smem_raw[];
     char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     char* sQ = smem;                                  // 32 KB
@@ -169,6 +170,7 @@ __global__ void __launch_bounds__(192, 1) attn_prefill_tc_kernel(const __grid_co
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = B->tmem;
+    pdl_wait();   // Q and the caches are written by the preceding kernels
 
     if (warp == 0) {
         if (lane == 0) {   // ---- TMA producer
@@ -435,6 +437,7 @@ __global__ void __launch_bounds__(320, 1) attn_prefill_tc2_kernel(const __grid_c
                                                                   const __grid_constant__ CUtensorMap tmV, int T,
                                                                   int HQ, int HKV, int pos0, bf16_t* __restrict__ O,
                                                                   float scale_log2) {
+    pdl_trigger();
     extern __shared__ __align__(1024) char smem_raw[];
     char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     char* sQ = smem;                                  // 2 heads x 32 KB
@@ -476,6 +479,7 @@ __global__ void __launch_bounds__(320, 1) attn_prefill_tc2_kernel(const __grid_c
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = B->tmem;
+    pdl_wait();   // Q and the caches are written by the preceding kernels
 
     if (warp == 0) {
         if (lane == 0) {   // ---- TMA producer: items in consumption order K0, K1, V0, K2, V1, ...
@@ -803,9 +807,8 @@ cudaError_t launch_attention_prefill_tc(const bf16_t* Q, int T, const Shape& sh,
             attr2 = true;
         }
         // x = head pair, y = query tile rank: CTAs are dispatched longest causal rows first
-        attn_prefill_tc2_kernel<<<dim3(sh.HQ / 2, ntq), 320, smem, s>>>(mq, mk, mv, T, sh.HQ, sh.HKV, pos0, O,
-                                                                         scale_log2);
-        return cudaGetLastError();
+        return launch_pdl(attn_prefill_tc2_kernel, dim3(sh.HQ / 2, ntq), dim3(320), smem, s, mq, mk, mv, T, sh.HQ,
+                          sh.HKV, pos0, O, scale_log2);
     }
     static bool attr = false;
     if (!attr) {
@@ -813,8 +816,8 @@ cudaError_t launch_attention_prefill_tc(const bf16_t* Q, int T, const Shape& sh,
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    attn_prefill_tc_kernel<<<dim3(ntq, sh.HQ), 192, smem, s>>>(mq, mk, mv, T, sh.HQ, sh.HKV, pos0, O, scale_log2, 1);
-    return cudaGetLastError();
+    return launch_pdl(attn_prefill_tc_kernel, dim3(ntq, sh.HQ), dim3(192), smem, s, mq, mk, mv, T, sh.HQ, sh.HKV, pos0,
+                      O, scale_log2, 1);
 }
 
 cudaError_t launch_attention_bidir_tc(const bf16_t* Q, const bf16_t* K, const bf16_t* V, int row_stride, int T,
@@ -837,8 +840,8 @@ cudaError_t launch_attention_bidir_tc(const bf16_t* Q, const bf16_t* K, const bf
     }
     const float scale_log2 = 1.4426950408889634f / sqrtf(128.f);
     const int ntq = (T + QT - 1) / QT;
-    attn_prefill_tc_kernel<<<dim3(ntq, heads), 192, smem, s>>>(mq, mk, mv, T, heads, heads, 0, O, scale_log2, 0);
-    return cudaGetLastError();
+    return launch_pdl(attn_prefill_tc_kernel, dim3(ntq, heads), dim3(192), smem, s, mq, mk, mv, T, heads, heads, 0, O,
+                      scale_log2, 0);
 }
 
 }  // namespace qdec

@@ -243,6 +243,8 @@ __global__ void batch_attn_merge_kernel(int HQ, int D, int n_split_own, int n_sp
 // One thread per pair of columns (F even) over all n rows.
 __global__ void batch_swiglu_kernel(const float* __restrict__ gu, int F, int n, bf16_t* __restrict__ h, int splits,
                                     size_t pstride) {
+    pdl_trigger();
+    pdl_wait();
     const int idx = blockIdx.x * blockDim.x + threadIdx.x;   // pair index
     const int half = F >> 1;
     if (idx >= n * half) return;
@@ -358,8 +360,7 @@ cudaError_t launch_batch_swiglu(const float* gu, int F, int n, bf16_t* h, cudaSt
     (void)cudaGetLastError();
     if (F % 2 != 0 || splits < 1 || pstride % 2 != 0) return cudaErrorInvalidValue;
     const int pairs = n * (F / 2);
-    batch_swiglu_kernel<<<(pairs + 255) / 256, 256, 0, st>>>(gu, F, n, h, splits, pstride);
-    return cudaGetLastError();
+    return launch_pdl(batch_swiglu_kernel, dim3((pairs + 255) / 256), dim3(256), 0, st, gu, F, n, h, splits, pstride);
 }
 
 cudaError_t launch_batch_argmax(const float* logits, int V, int ld, const BatchStream* bs, int n, int* out,

@@ -10,10 +10,22 @@
 
 namespace qdec {
 
+namespace {
+int g_programmatic = 1;
+}
+int set_programmatic_launch(int on) {
+    const int prev = g_programmatic;
+    g_programmatic = on ? 1 : 0;
+    return prev;
+}
+bool programmatic_launch() { return g_programmatic != 0; }
+
 // One block per row; 8-byte loads of 4 bf16, 16-byte stores of 4 fp32.
 __global__ void embed_splice_kernel(const bf16_t* __restrict__ E, const int* __restrict__ ids, int H,
                                     const bf16_t* __restrict__ audio, int n_audio, int off,
                                     float* __restrict__ X, int* __restrict__ history) {
+    pdl_trigger();
+    pdl_wait();
     const int t = blockIdx.x;
     const bool is_audio = (t >= off) && (t < off + n_audio);
     const int id = ids[t];
@@ -29,8 +41,7 @@ __global__ void embed_splice_kernel(const bf16_t* __restrict__ E, const int* __r
 cudaError_t launch_embed_splice(const bf16_t* E, const int* ids_dev, int T, int H, const bf16_t* audio,
                                 int n_audio, int off, float* X, int* history, cudaStream_t s) {
     (void)cudaGetLastError();   // attribute only this launch's errors
-    embed_splice_kernel<<<T, 128, 0, s>>>(E, ids_dev, H, audio, n_audio, off, X, history);
-    return cudaGetLastError();
+    return launch_pdl(embed_splice_kernel, dim3(T), dim3(128), 0, s, E, ids_dev, H, audio, n_audio, off, X, history);
 }
 
 // Decode embedding: token >= 0 is embedded; -1 embeds the previous step's argmax (greedy
@@ -55,12 +66,15 @@ cudaError_t launch_embed_token(const bf16_t* E, int token, const int* prev_argma
 }
 
 __global__ void advance_position_kernel(int* pos, int n) { *pos += n; }
-__global__ void set_int_kernel(int* p, int v) { *p = v; }
+__global__ void set_int_kernel(int* p, int v) {
+    pdl_trigger();
+    pdl_wait();
+    *p = v;
+}
 
 cudaError_t launch_set_int(int* p, int v, cudaStream_t s) {
     (void)cudaGetLastError();   // attribute only this launch's errors
-    set_int_kernel<<<1, 1, 0, s>>>(p, v);
-    return cudaGetLastError();
+    return launch_pdl(set_int_kernel, dim3(1), dim3(1), 0, s, p, v);
 }
 
 cudaError_t launch_advance_position(int* pos, int n, cudaStream_t s) {
@@ -82,6 +96,8 @@ __device__ __forceinline__ float block_sum_256(float v, float* red) {
 
 __global__ void rmsnorm_bf16_kernel(const float* __restrict__ X, int H, const bf16_t* __restrict__ g,
                                     float eps, bf16_t* __restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float red[8];
     const float* x = X + (size_t)blockIdx.x * H;
     float ss = 0.f;
@@ -108,6 +124,8 @@ __global__ void rmsnorm_bf16_kernel(const float* __restrict__ X, int H, const bf
 __global__ void __launch_bounds__(128) rmsnorm1024_bf16_kernel(const float* __restrict__ X,
                                                                const bf16_t* __restrict__ g, float eps,
                                                                bf16_t* __restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float red[4];
     const float4* x = reinterpret_cast<const float4*>(X + (size_t)blockIdx.x * 1024);
     const int t = threadIdx.x;
@@ -128,11 +146,8 @@ __global__ void __launch_bounds__(128) rmsnorm1024_bf16_kernel(const float* __re
 cudaError_t launch_rmsnorm_bf16(const float* X, int T, int H, const bf16_t* g, float eps, bf16_t* out,
                                 cudaStream_t s) {
     (void)cudaGetLastError();   // attribute only this launch's errors
-    if (H == 1024)
-        rmsnorm1024_bf16_kernel<<<T, 128, 0, s>>>(X, g, eps, out);
-    else
-        rmsnorm_bf16_kernel<<<T, 256, 0, s>>>(X, H, g, eps, out);
-    return cudaGetLastError();
+    if (H == 1024) return launch_pdl(rmsnorm1024_bf16_kernel, dim3(T), dim3(128), 0, s, X, g, eps, out);
+    return launch_pdl(rmsnorm_bf16_kernel, dim3(T), dim3(256), 0, s, X, H, g, eps, out);
 }
 
 // rmsnorm_bf16_kernel after folding split-K partials into the residual row: each thread
@@ -140,6 +155,8 @@ cudaError_t launch_rmsnorm_bf16(const float* X, int T, int H, const bf16_t* g, f
 __global__ void rmsnorm_fold_bf16_kernel(float* __restrict__ X, const float* __restrict__ part, int splits,
                                          size_t pstride, int H, const bf16_t* __restrict__ g, float eps,
                                          bf16_t* __restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float red[8];
     float* x = X + (size_t)blockIdx.x * H;
     const float* pr = part + (size_t)blockIdx.x * H;
@@ -170,12 +187,13 @@ cudaError_t launch_rmsnorm_fold_bf16(float* X, const float* part, int splits, si
                                      const bf16_t* g, float eps, bf16_t* out, cudaStream_t s) {
     (void)cudaGetLastError();   // attribute only this launch's errors
     if (H % 4 != 0 || pstride % 4 != 0 || splits < 1) return cudaErrorInvalidValue;
-    rmsnorm_fold_bf16_kernel<<<T, 256, 0, s>>>(X, part, splits, pstride, H, g, eps, out);
-    return cudaGetLastError();
+    return launch_pdl(rmsnorm_fold_bf16_kernel, dim3(T), dim3(256), 0, s, X, part, splits, pstride, H, g, eps, out);
 }
 
 __global__ void fold_partials_kernel(float* __restrict__ X, const float* __restrict__ part, int splits,
                                      size_t pstride, size_t n) {
+    pdl_trigger();
+    pdl_wait();
     const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     float v = X[i];
@@ -185,8 +203,8 @@ __global__ void fold_partials_kernel(float* __restrict__ X, const float* __restr
 
 cudaError_t launch_fold_partials(float* X, const float* part, int splits, size_t pstride, size_t n, cudaStream_t s) {
     (void)cudaGetLastError();   // attribute only this launch's errors
-    fold_partials_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(X, part, splits, pstride, n);
-    return cudaGetLastError();
+    return launch_pdl(fold_partials_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, X, part, splits, pstride,
+                      n);
 }
 
 // grid (T, HQ + 2 HKV), block max(32, D/2): thread i < D/2 owns the NeoX pair (i, i + D/2) of one head.
@@ -197,6 +215,8 @@ __global__ void qk_norm_rope_append_kernel(const float* __restrict__ qkv, int HQ
                                            bf16_t* __restrict__ q_bf16, float* __restrict__ q_f32,
                                            bf16_t* __restrict__ k_cache, bf16_t* __restrict__ v_cache,
                                            int splits, size_t pstride) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float red[4];
     const int t = blockIdx.x, hh = blockIdx.y, i = threadIdx.x, half = D >> 1;
     const int rows = (HQ + 2 * HKV) * D;
@@ -258,10 +278,9 @@ cudaError_t launch_qk_norm_rope_append(const float* qkv, int T, const Shape& sh,
     (void)cudaGetLastError();   // attribute only this launch's errors
     if (splits < 1) return cudaErrorInvalidValue;
     dim3 grid(T, sh.HQ + 2 * sh.HKV);
-    qk_norm_rope_append_kernel<<<grid, sh.D / 2 < 32 ? 32 : sh.D / 2, 0, s>>>(qkv, sh.HQ, sh.HKV, sh.D, sh.max_seq, sh.eps, pos0,
-                                                         g_q, g_k, rope_cs, q_bf16, q_f32, k_cache, v_cache,
-                                                         splits, pstride);
-    return cudaGetLastError();
+    return launch_pdl(qk_norm_rope_append_kernel, grid, dim3(sh.D / 2 < 32 ? 32 : sh.D / 2), 0, s, qkv, sh.HQ, sh.HKV,
+                      sh.D, sh.max_seq, sh.eps, pos0, g_q, g_k, rope_cs, q_bf16, q_f32, k_cache, v_cache, splits,
+                      pstride);
 }
 
 }  // namespace qdec

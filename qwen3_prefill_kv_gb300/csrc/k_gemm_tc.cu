@@ -444,6 +444,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tc_kernel(const __grid_c
                                                          bf16_t* __restrict__ Cb, int ldc, const QkvRopeEpi epi,
                                                          int tiles_m, int tiles_n, int splits,
                                                          const float* __restrict__ bias, int relu) {
+    pdl_trigger();
     extern __shared__ __align__(1024) char smem_raw[];
     char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     constexpr int A_BYTES = BM * BK * 2;
@@ -495,9 +496,30 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tc_kernel(const __grid_c
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    if (warp != 0) pdl_wait();   // the producer waits after requesting its first weight tiles
 
     if (warp == 0) {
         if (lane == 0) {   // ---- TMA producer: one stage ring across all of this CTA's units
+            // B: BN rows in boxes of B_BOX rows stacked in shared memory (SwiGLU: the gate
+            // rows, then the matching up rows)
+            auto load_b = [&](uint32_t s, int n0, int kb) {
+#pragma unroll
+                for (int b = 0; b < B_LOADS; ++b)
+                    tma_2d(sB + s * B_BYTES + b * B_BOX * 128, &tmB, kb * BK,
+                           GLU ? (b ? up_off + n0 : n0) : n0 + b * B_BOX, &full[s]);
+            };
+            // The weights do not depend on the preceding kernel: the B tiles of the first
+            // stages are requested before waiting for it, their A tiles after.
+            uint32_t npre = 0;
+            for (int u = blockIdx.x; u < units && npre < (uint32_t)STAGES; u += gridDim.x) {
+                int m0, nt, kb0, nk, z;
+                unit(u, m0, nt, kb0, nk, z);
+                for (int kb = 0; kb < nk && npre < (uint32_t)STAGES; ++kb, ++npre) {
+                    mb_expect(&full[npre], A_BYTES + B_BYTES);
+                    load_b(npre, nt * (GLU ? BN / 2 : BN), kb0 + kb);
+                }
+            }
+            pdl_wait();
             uint32_t g = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
@@ -506,18 +528,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tc_kernel(const __grid_c
                 const int n0 = nt * (GLU ? BN / 2 : BN);
                 for (int kb = 0; kb < nk; ++kb, ++g) {
                     const uint32_t s = g % STAGES, r = g / STAGES;
-                    if (!mb_wait_ab(&empty[s], (r & 1) ^ 1, 1, abort)) {
-                        ok = false;
-                        break;
+                    if (g >= npre) {
+                        if (!mb_wait_ab(&empty[s], (r & 1) ^ 1, 1, abort)) {
+                            ok = false;
+                            break;
+                        }
+                        mb_expect(&full[s], A_BYTES + B_BYTES);
+                        load_b(s, n0, kb0 + kb);
                     }
-                    mb_expect(&full[s], A_BYTES + B_BYTES);
                     tma_2d(sA + s * A_BYTES, &tmA, (kb0 + kb) * BK, m0, &full[s]);
-                    // B: BN rows in boxes of B_BOX rows stacked in shared memory (SwiGLU: the
-                    // gate rows, then the matching up rows)
-#pragma unroll
-                    for (int b = 0; b < B_LOADS; ++b)
-                        tma_2d(sB + s * B_BYTES + b * B_BOX * 128, &tmB, (kb0 + kb) * BK,
-                               GLU ? (b ? up_off + n0 : n0) : n0 + b * B_BOX, &full[s]);
                 }
             }
             // the last copies issued must land before the CTA exits (after an error they may not
@@ -600,6 +619,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
                     const __grid_constant__ CUtensorMap tmC, int M, int K,
                     int up_off, float* __restrict__ Cf, bf16_t* __restrict__ Cb, int ldc, const QkvRopeEpi epi,
                     int tiles_m, int tiles_n, const float* __restrict__ bias, int relu) {
+    pdl_trigger();
     extern __shared__ __align__(1024) char smem_raw[];
     char* smem = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     constexpr int BN = 256;
@@ -641,24 +661,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     cluster_sync();   // both CTAs' barriers are initialised before either signals the other's
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    if (warp != 0) pdl_wait();   // the producer waits after requesting its first weight tiles
 
     if (warp == 0) {
         if (lane == 0) {   // ---- TMA producer of this CTA's halves
+            auto b0_of = [&](int nt) { return GLU ? (rank ? up_off : 0) + nt * 128 : nt * BN + (int)rank * 128; };
+            // the B tiles of the first stages before waiting for the preceding kernel, as in
+            // gemm_tc_kernel
+            uint32_t npre = 0;
+            for (int u = pair; u < units && npre < (uint32_t)STAGES; u += npairs)
+                for (int kb = 0; kb < nkb && npre < (uint32_t)STAGES; ++kb, ++npre) {
+                    if (rank == 0) mb_expect(&full[npre], 2 * (A_BYTES + B_BYTES));
+                    tma_2d_pair(sB + npre * B_BYTES, &tmB, kb * BK, b0_of(u / tiles_m), peer_addr(&full[npre], 0));
+                }
+            pdl_wait();
             uint32_t g = 0;
             bool ok = true;
             for (int u = pair; u < units && ok; u += npairs) {
                 const int m0 = (u % tiles_m) * 2 * BM + (int)rank * BM, nt = u / tiles_m;
-                const int b0 = GLU ? (rank ? up_off : 0) + nt * 128 : nt * BN + (int)rank * 128;
                 for (int kb = 0; kb < nkb; ++kb, ++g) {
                     const uint32_t s = g % STAGES, r = g / STAGES;
-                    if (!mb_wait_ab(&empty[s], (r & 1) ^ 1, 1, abort)) {
-                        ok = false;
-                        break;
-                    }
                     const uint32_t fb = peer_addr(&full[s], 0);
-                    if (rank == 0) mb_expect(&full[s], 2 * (A_BYTES + B_BYTES));
+                    if (g >= npre) {
+                        if (!mb_wait_ab(&empty[s], (r & 1) ^ 1, 1, abort)) {
+                            ok = false;
+                            break;
+                        }
+                        if (rank == 0) mb_expect(&full[s], 2 * (A_BYTES + B_BYTES));
+                        tma_2d_pair(sB + s * B_BYTES, &tmB, kb * BK, b0_of(nt), fb);
+                    }
                     tma_2d_pair(sA + s * A_BYTES, &tmA, kb * BK, m0, fb);
-                    tma_2d_pair(sB + s * B_BYTES, &tmB, kb * BK, b0, fb);
                 }
             }
             // the last copies issued must land before the CTA exits: CTA 0 sees them on its
@@ -795,9 +827,8 @@ cudaError_t launch_bn(const CUtensorMap& ma, const CUtensorMap& mb, const CUtens
     const int tiles_m = (M + BM - 1) / BM, tiles_n = N / tile_n;
     const long long units = (long long)tiles_m * tiles_n * splits;
     const int grid = (int)(units < resident ? units : resident);   // persistent: each CTA walks units
-    kern<<<grid, GEMM_THREADS, smem, s>>>(ma, mb, mc, M, K, up_off, Cf, Cb, ldc, epi, tiles_m, tiles_n, splits, bias,
-                                          relu);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(GEMM_THREADS), smem, s, ma, mb, mc, M, K, up_off, Cf, Cb, ldc, epi,
+                      tiles_m, tiles_n, splits, bias, relu);
 }
 
 // Tile width.  A 128 x 256 tile moves 1.33x fewer operand bytes per FLOP than a 128 x 128 one,
@@ -851,8 +882,8 @@ cudaError_t launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUte
     const int tiles_m = (M + 2 * BM - 1) / (2 * BM), tiles_n = N / (MODE == GEMM_SWIGLU_BF16 ? 128 : 256);
     const long long units = (long long)tiles_m * tiles_n;
     const int grid = 2 * (int)(units < pairs ? units : pairs);   // persistent: each pair walks units
-    kern<<<grid, GEMM_THREADS, smem, s>>>(ma, mb, mc, M, K, up_off, Cf, Cb, ldc, epi, tiles_m, tiles_n, bias, relu);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(GEMM_THREADS), smem, s, ma, mb, mc, M, K, up_off, Cf, Cb, ldc, epi,
+                      tiles_m, tiles_n, bias, relu);
 }
 
 // Tile height of the 256-wide tiles.  A CTA pair (256 x 256) moves 1.5x fewer operand bytes

@@ -107,6 +107,8 @@ __global__ void __launch_bounds__(GEMV_THREADS) lm_head_argmax_kernel(const bf16
     __shared__ float bv[GEMV_THREADS / 32];
     __shared__ int bi[GEMV_THREADS / 32];
     __shared__ bool last;
+    pdl_trigger();
+    pdl_wait();
     load_x(xs, x, H, g, eps, red);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row0 = (blockIdx.x * (GEMV_THREADS / 32) + warp) * LM_R;
@@ -204,9 +206,8 @@ cudaError_t launch_lm_head_argmax(const bf16_t* E, int V, int H, const float* x,
     (void)cudaGetLastError();   // attribute only this launch's errors
     if (H % 8 != 0) return cudaErrorInvalidValue;
     const int grid = (V + LM_ROWS_PER_BLOCK - 1) / LM_ROWS_PER_BLOCK;
-    lm_head_argmax_kernel<<<grid, GEMV_THREADS, (size_t)H * sizeof(float), s>>>(E, V, H, x, g_final, eps, logits,
-                                                                                 argmax, scratch);
-    return cudaGetLastError();
+    return launch_pdl(lm_head_argmax_kernel, dim3(grid), dim3(GEMV_THREADS), (size_t)H * sizeof(float), s, E, V, H, x,
+                      g_final, eps, logits, argmax, scratch);
 }
 
 }  // namespace qdec

@@ -49,6 +49,11 @@ int qdec_op_gemm_splitk(const void* A, int32_t lda, const void* W, int32_t M, in
                                       GEMM_ATOMIC_F32, 0, C, nullptr, ldc, static_cast<cudaStream_t>(stream), splits));
 }
 
+int qdec_op_programmatic_launch(int32_t on) {
+    if (on != 0 && on != 1) return set_error(QDEC_E_INVALID_ARG, "qdec_op_programmatic_launch: %d is not 0 or 1", on);
+    return set_programmatic_launch(on);
+}
+
 int qdec_op_gemm_tile_rows(int32_t bm) {
     if (bm != 0 && bm != 128 && bm != 256)
         return set_error(QDEC_E_INVALID_ARG, "qdec_op_gemm_tile_rows: %d is not 0, 128 or 256", bm);

@@ -145,6 +145,41 @@ def test_mid_length_prefill(full):
             np.testing.assert_allclose(a, b, rtol=0, atol=2e-2 * float(np.abs(b).max()), err_msg=f"{layer} {kind}")
 
 
+@pytest.mark.parametrize("name", ["funasr_nano_short", "qwen3_asr_30s", "long_context"])
+def test_programmatic_launch_is_bit_identical(full, name):
+    """The prefill chain launched with programmatic dependent launch (each kernel starts its
+    prologue and first weight loads while the previous one finishes, then waits for it) and
+    launched plainly must give the same bits: logits of the eager run, the captured run and
+    the graph replay, and every layer's K and V slots.  64 positions take the split-K paths,
+    415 a mix, 4096 the unsplit 128 x 256 tiles."""
+    w, wd, orc = full
+    wl = synth.WORKLOADS[name]
+    p = synth.make_prompt(wl, seed=0)
+    runs = []
+    for on in (1, 0):
+        prev = _lib.programmatic_launch(on)
+        try:
+            d = Decoder(SH, wd, max_seq=wl.n_prompt + 1)
+            lg = torch.empty(SH.vocab, device="cuda")
+            logits = []
+            for _ in range(3):   # eager, captured into a graph, replayed
+                d.prefill(p.ids, p.audio.cuda(), p.audio_offset, logits=lg)
+                d.sync()
+                logits.append(lg.cpu().numpy().copy())
+            _lib.device_error()
+            kv = [d.read_kv(l, k, 0, wl.n_prompt) for l in range(SH.n_layers) for k in (0, 1)]
+            d.close()
+        finally:
+            _lib.programmatic_launch(prev)
+        runs.append((logits, kv))
+    (la, ka), (lb, kb) = runs
+    for i in range(3):
+        assert np.array_equal(la[i].view(np.uint32), lb[i].view(np.uint32)), f"logits of run {i}"
+        assert np.array_equal(la[i].view(np.uint32), la[0].view(np.uint32)), f"run {i} against the eager run"
+    for i, (a, b) in enumerate(zip(ka, kb)):
+        assert np.array_equal(a, b), f"layer {i // 2} kind {i % 2}"
+
+
 @pytest.mark.slow
 def test_long_context_prefill_and_steps(full):
     w, wd, orc = full
