@@ -57,8 +57,10 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
-// silu(z) = z / (1 + e^-z)
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+// silu(z) = z / (1 + e^-z), with CUDA's fast exponential and division: every use rounds the
+// result (or its product with the up projection) to bf16, far coarser than their error of
+// a few ulp; for z below about -87 the quotient is 0, as silu's value there is below fp32's.
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 // (value, index) with "greater value wins, lower index wins a tie"; NaN never wins.
 struct ArgMax { float v; int i; };

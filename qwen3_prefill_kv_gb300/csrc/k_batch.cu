@@ -15,6 +15,8 @@ namespace {
 // Token of stream i: the forced token, or the stream's previous argmax when it is -1.
 __global__ void batch_embed_kernel(const bf16_t* __restrict__ E, int H, const int* __restrict__ tokens,
                                    const BatchStream* __restrict__ bs, float* __restrict__ X) {
+    pdl_trigger();
+    pdl_wait();
     const int i = blockIdx.x;
     const int t0 = tokens[i];
     const int id = t0 >= 0 ? t0 : *bs[i].argmax;
@@ -32,6 +34,8 @@ __global__ void batch_embed_kernel(const bf16_t* __restrict__ E, int H, const in
 __global__ void batch_qk_rope_kernel(const float* __restrict__ qkv, int HQ, int HKV, int D, float eps, int layer,
                                      const bf16_t* __restrict__ g_q, const bf16_t* __restrict__ g_k,
                                      const BatchStream* __restrict__ bs, float* __restrict__ q_out) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float red[4];
     const int s = blockIdx.x, hh = blockIdx.y, i = threadIdx.x, half = D >> 1;
     const int rows = (HQ + 2 * HKV) * D;
@@ -111,6 +115,8 @@ __global__ void __launch_bounds__(BNT) batch_attn_kernel(const float* __restrict
                                                          const BatchStream* __restrict__ bs, int n_split,
                                                          int n_split_total, float* __restrict__ part_ml,
                                                          float* __restrict__ part_o) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int EPL = D / 32;
     __shared__ float sm[BWARPS][G];
     __shared__ float sl[BWARPS][G];
@@ -221,6 +227,8 @@ __global__ void __launch_bounds__(BNT) batch_attn_kernel(const float* __restrict
 __global__ void batch_attn_merge_kernel(int HQ, int D, int n_split_own, int n_split_total,
                                         const BatchStream* __restrict__ bs, const float* __restrict__ part_ml,
                                         const float* __restrict__ part_o, bf16_t* __restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
     const int h = blockIdx.x, s = blockIdx.y;
     const size_t base = ((size_t)s * HQ + h) * n_split_total;
     const int n_split = bs[s].shared > 0 ? n_split_total : n_split_own;
@@ -263,6 +271,8 @@ __global__ void batch_swiglu_kernel(const float* __restrict__ gu, int F, int n, 
 // then the stream's position advances.
 __global__ void batch_argmax_kernel(const float* __restrict__ logits, int V, int ld, const BatchStream* __restrict__ bs,
                                     int* __restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float bv[32];
     __shared__ int bi[32];
     const int s = blockIdx.x;
@@ -308,13 +318,12 @@ cudaError_t launch_attn_d(const float* q, int HQ, int HKV, int layer, const Batc
                           int nst, float* part_ml, float* part_o, cudaStream_t st) {
     dim3 grid(HKV, n_split, n);
     switch (HQ / HKV) {
-        case 1: batch_attn_kernel<D, 1><<<grid, BNT, 0, st>>>(q, HQ, HKV, layer, bs, n_split, nst, part_ml, part_o); break;
-        case 2: batch_attn_kernel<D, 2><<<grid, BNT, 0, st>>>(q, HQ, HKV, layer, bs, n_split, nst, part_ml, part_o); break;
-        case 4: batch_attn_kernel<D, 4><<<grid, BNT, 0, st>>>(q, HQ, HKV, layer, bs, n_split, nst, part_ml, part_o); break;
-        case 8: batch_attn_kernel<D, 8><<<grid, BNT, 0, st>>>(q, HQ, HKV, layer, bs, n_split, nst, part_ml, part_o); break;
+        case 1: return launch_pdl(batch_attn_kernel<D, 1>, grid, dim3(BNT), 0, st, q, HQ, HKV, layer, bs, n_split, nst, part_ml, part_o);
+        case 2: return launch_pdl(batch_attn_kernel<D, 2>, grid, dim3(BNT), 0, st, q, HQ, HKV, layer, bs, n_split, nst, part_ml, part_o);
+        case 4: return launch_pdl(batch_attn_kernel<D, 4>, grid, dim3(BNT), 0, st, q, HQ, HKV, layer, bs, n_split, nst, part_ml, part_o);
+        case 8: return launch_pdl(batch_attn_kernel<D, 8>, grid, dim3(BNT), 0, st, q, HQ, HKV, layer, bs, n_split, nst, part_ml, part_o);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace
@@ -322,17 +331,15 @@ cudaError_t launch_attn_d(const float* q, int HQ, int HKV, int layer, const Batc
 cudaError_t launch_batch_embed(const bf16_t* E, int H, const int* tokens, const BatchStream* bs, int n, float* X,
                                cudaStream_t st) {
     (void)cudaGetLastError();
-    batch_embed_kernel<<<n, 128, 0, st>>>(E, H, tokens, bs, X);
-    return cudaGetLastError();
+    return launch_pdl(batch_embed_kernel, dim3(n), dim3(128), 0, st, E, H, tokens, bs, X);
 }
 
 cudaError_t launch_batch_qk_rope(const float* qkv, const Shape& sh, int layer, const bf16_t* g_q, const bf16_t* g_k,
                                  const BatchStream* bs, int n, float* q_out, cudaStream_t st) {
     (void)cudaGetLastError();
     dim3 grid(n, sh.HQ + 2 * sh.HKV);
-    batch_qk_rope_kernel<<<grid, sh.D / 2 < 32 ? 32 : sh.D / 2, 0, st>>>(qkv, sh.HQ, sh.HKV, sh.D, sh.eps, layer, g_q,
-                                                                        g_k, bs, q_out);
-    return cudaGetLastError();
+    return launch_pdl(batch_qk_rope_kernel, grid, dim3(sh.D / 2 < 32 ? 32 : sh.D / 2), 0, st, qkv, sh.HQ, sh.HKV, sh.D,
+                      sh.eps, layer, g_q, g_k, bs, q_out);
 }
 
 cudaError_t launch_batch_attention(const float* q, const Shape& sh, int layer, const BatchStream* bs, int n, int n_split,
@@ -352,8 +359,8 @@ cudaError_t launch_batch_attention(const float* q, const Shape& sh, int layer, c
         e = launch_prefix_attention(q, sh, layer, items, n_items, members, max_chunks, nst, n_split, part_ml, part_o, st);
         if (e != cudaSuccess) return e;
     }
-    batch_attn_merge_kernel<<<dim3(sh.HQ, n), 128, 0, st>>>(sh.HQ, sh.D, n_split, nst, bs, part_ml, part_o, out);
-    return cudaGetLastError();
+    return launch_pdl(batch_attn_merge_kernel, dim3(sh.HQ, n), dim3(128), 0, st, sh.HQ, sh.D, n_split, nst, bs, part_ml,
+                      part_o, out);
 }
 
 cudaError_t launch_batch_swiglu(const float* gu, int F, int n, bf16_t* h, cudaStream_t st, int splits, size_t pstride) {
@@ -366,8 +373,7 @@ cudaError_t launch_batch_swiglu(const float* gu, int F, int n, bf16_t* h, cudaSt
 cudaError_t launch_batch_argmax(const float* logits, int V, int ld, const BatchStream* bs, int n, int* out,
                                 cudaStream_t st) {
     (void)cudaGetLastError();
-    batch_argmax_kernel<<<n, 1024, 0, st>>>(logits, V, ld, bs, out);
-    return cudaGetLastError();
+    return launch_pdl(batch_argmax_kernel, dim3(n), dim3(1024), 0, st, logits, V, ld, bs, out);
 }
 
 }  // namespace qdec

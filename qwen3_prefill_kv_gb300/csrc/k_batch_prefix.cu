@@ -62,6 +62,8 @@ __global__ void __launch_bounds__(PX_THREADS) prefix_attn_kernel(const float* __
                                                                   const int* __restrict__ members, int n_split_total,
                                                                   int split0, float* __restrict__ part_ml,
                                                                   float* __restrict__ part_o) {
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ __align__(1024) unsigned char px_smem[];
     unsigned char* Qs = px_smem;                              // [128 rows][128] bf16, swizzled
     unsigned char* Ks = px_smem + PX_ROWS * 256;              // [32 keys][128]
@@ -239,9 +241,8 @@ cudaError_t launch_prefix_attention(const float* q, const Shape& sh, int layer, 
             if (e != cudaSuccess) return e;                                                                      \
             attr = true;                                                                                         \
         }                                                                                                        \
-        prefix_attn_kernel<GG><<<grid, PX_THREADS, smem, st>>>(q, sh.HQ, sh.HKV, layer, sh.max_seq, items, members, \
-                                                              n_split_total, split0, part_ml, part_o);         \
-        break;                                                                                                   \
+        return launch_pdl(prefix_attn_kernel<GG>, grid, dim3(PX_THREADS), smem, st, q, sh.HQ, sh.HKV, layer,       \
+                          sh.max_seq, items, members, n_split_total, split0, part_ml, part_o);                   \
     }
         PX_CASE(1)
         PX_CASE(2)
@@ -250,7 +251,6 @@ cudaError_t launch_prefix_attention(const float* q, const Shape& sh, int layer, 
 #undef PX_CASE
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace qdec

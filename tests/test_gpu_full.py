@@ -59,7 +59,7 @@ def test_teacher_forced_workload(full, name):
 
 
 @pytest.mark.parametrize("name,tile", [("funasr_nano_short", 0), ("qwen3_asr_30s", 0), ("qwen3_asr_30s", 256),
-                                       ("qwen3_asr_30s", 256256)])
+                                       ("qwen3_asr_30s", 256256), ("qwen3_asr_30s", 128)])
 def test_fused_qkv_epilogue_matches_separate_kernels(full, name, tile):
     """The tcgen05 prefill writes K and V from the QKV GEMM's epilogue (per-head norm + RoPE
     fused); the CUDA-core prefill runs the GEMM and the norm/RoPE/append kernel separately.
@@ -91,6 +91,8 @@ def test_fused_qkv_epilogue_matches_separate_kernels(full, name, tile):
             fa, fb = a.view(np.float32), b.view(np.float32)
             np.testing.assert_allclose(fa, fb, rtol=0, atol=1e-2 * float(np.abs(fb).max()),
                                        err_msg=f"layer {layer} kind {kind}")
+            # the epilogue's bulk stores end at the prompt: the slot after it is still zero
+            assert not decs[0].read_kv(layer, kind, wl.n_prompt, 1).any(), f"layer {layer} kind {kind}"
     np.testing.assert_allclose(logits[0], logits[1], rtol=0, atol=1e-2 * float(np.abs(logits[1]).max()))
 
 
