@@ -155,7 +155,7 @@ struct qdec_ctx {
 
     // persistent device state
     bf16_t* kv = nullptr;        // [NL][2][HKV][max_seq][D]
-    float2* rope = nullptr;      // [max_seq][D/2] (cos, sin)
+    float2* rope = nullptr;      // [max_seq][D/2] (cos, sin), then the same values as [D/2][max_seq]
     int* d_hist = nullptr;       // [max_seq]
     int* d_pos = nullptr;        // position of the next token
     int* d_zero = nullptr;       // constant 0 (prefill start position)
@@ -291,7 +291,7 @@ int alloc_state(qdec_ctx* c) {
     CK(cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking));
     CK(dalloc(&c->kv, (size_t)sh.NL * c->kv_layer_stride()));
     CK(cudaMemset(c->kv, 0, (size_t)sh.NL * c->kv_layer_stride() * sizeof(bf16_t)));
-    CK(dalloc(&c->rope, (size_t)sh.max_seq * (sh.D / 2)));
+    CK(dalloc(&c->rope, 2 * (size_t)sh.max_seq * (sh.D / 2)));
     CK(dalloc(&c->d_hist, (size_t)sh.max_seq));
     CK(dalloc(&c->d_pos, 1));
     CK(dalloc(&c->d_zero, 1));
@@ -399,14 +399,19 @@ int set_weight_format(qdec_ctx* c, int fmt) {
     return QDEC_OK;
 }
 
+// (cos, sin) of position p and NeoX pair i, by position ([max_seq][D/2]: the pairs of one
+// position contiguous) and then by pair ([D/2][max_seq]: consecutive positions contiguous, for
+// the prefill epilogue whose threads own consecutive positions).
 int build_rope_table(qdec_ctx* c) {
-    const int half = c->sh.D / 2;
-    std::vector<float2> t((size_t)c->sh.max_seq * half);
-    for (int p = 0; p < c->sh.max_seq; ++p)
+    const int half = c->sh.D / 2, S = c->sh.max_seq;
+    std::vector<float2> t(2 * (size_t)S * half);
+    for (int p = 0; p < S; ++p)
         for (int i = 0; i < half; ++i) {
             const double inv = std::pow((double)c->cfg.rope_theta, -2.0 * i / (double)c->sh.D);
             const double a = (double)p * inv;
-            t[(size_t)p * half + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+            const float2 v = make_float2((float)std::cos(a), (float)std::sin(a));
+            t[(size_t)p * half + i] = v;
+            t[(size_t)S * half + (size_t)i * S + p] = v;
         }
     CK(cudaMemcpy(c->rope, t.data(), t.size() * sizeof(float2), cudaMemcpyHostToDevice));
     return QDEC_OK;
@@ -503,7 +508,8 @@ int prefill_layer(qdec_ctx* c, int l, int T, int* fold, uint64_t* kernels, cudaS
         k += 2;
     } else if (c->prefill_gemm == QDEC_PREFILL_TCGEN05 && gemm_tc_qkv_rope_supported(sh, sh.H)) {
         // QKV projection with the per-head norm, RoPE and KV append in its epilogue
-        QkvRopeEpi e{c->rope, w.g_q, w.g_k, c->p_Q, c->k_cache(l), c->v_cache(l), 0, sh.HQ, sh.HKV, sh.max_seq, sh.eps};
+        QkvRopeEpi e{c->rope, c->rope + (size_t)sh.max_seq * (sh.D / 2), w.g_q, w.g_k, c->p_Q, c->k_cache(l),
+                     c->v_cache(l), 0, sh.HQ, sh.HKV, sh.max_seq, sh.eps};
         CK(launch_gemm_tc_qkv_rope(c->p_Xn, sh.H, w.wqkv, T, sh.H, e, s));
         k += 1;
     } else {
@@ -1144,7 +1150,7 @@ int qdec_clone(const qdec_ctx* src, qdec_ctx** out) {
                 e = cudaMemcpyAsync(c->d_hist, src->d_hist, L * sizeof(int), cudaMemcpyDeviceToDevice, c->stream);
         }
         if (e == cudaSuccess)
-            e = cudaMemcpyAsync(c->rope, src->rope, (size_t)sh.max_seq * (sh.D / 2) * sizeof(float2),
+            e = cudaMemcpyAsync(c->rope, src->rope, 2 * (size_t)sh.max_seq * (sh.D / 2) * sizeof(float2),
                                 cudaMemcpyDeviceToDevice, c->stream);
         if (e == cudaSuccess) e = cudaMemcpyAsync(c->d_pos, src->d_pos, sizeof(int), cudaMemcpyDeviceToDevice, c->stream);
         if (e == cudaSuccess)

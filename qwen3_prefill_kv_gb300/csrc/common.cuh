@@ -143,6 +143,7 @@ cudaError_t launch_gemm_tc(const bf16_t* A, int lda, const bf16_t* W, int M, int
 // k heads -> RMSNorm(g_k) + RoPE -> bf16 K cache slot pos0 + row; v heads -> bf16 V cache.
 struct QkvRopeEpi {
     const float2* rope;        // [max_seq][64] (cos, sin)
+    const float2* rope_t;      // the same values as [64][max_seq]
     const bf16_t *g_q, *g_k;   // [128]
     bf16_t *q, *kc, *vc;       // q [M][HQ][128]; this layer's K and V cache [HKV][max_seq][128]
     int pos0, HQ, HKV, max_seq;

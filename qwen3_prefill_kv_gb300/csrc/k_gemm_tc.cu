@@ -82,6 +82,20 @@ __device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x,
         "l"(map), "r"(x), "r"(y), "r"(s32(bar))
         : "memory");
 }
+// Weight tiles are loaded with an evict-first L2 policy: a prefill streams every layer's
+// weights through L2 once, and they should not push out the activations the next kernels read.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ void tma_2d_hint(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(
+            s32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(s32(bar)), "l"(pol)
+        : "memory");
+}
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(s32(slot)), "r"(ncols)
                  : "memory");
@@ -227,17 +241,19 @@ __device__ __forceinline__ void qkv_rope_block(uint32_t taddr, int c, float r, i
         dst = e.vc + ((size_t)(hd - e.HQ - e.HKV) * e.max_seq + p) * 128;
     } else {
         const bf16_t* g = hd < e.HQ ? e.g_q : e.g_k;
-        const float2* cs = e.rope + (size_t)p * 64 + c;
+        // (cos, sin) of pair c + i at this row's position from the pair-major table: the lanes
+        // own consecutive positions, so each load is contiguous across the warp
+        const float2* cs = e.rope_t + (size_t)c * e.max_seq + p;
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
             const uint32_t ga = *reinterpret_cast<const uint32_t*>(g + c + i);
             const uint32_t gb = *reinterpret_cast<const uint32_t*>(g + 64 + c + i);
-            const float4 c2 = *reinterpret_cast<const float4*>(cs + i);   // (cos, sin) of pairs c + i, c + i + 1
+            const float2 cs0 = cs[(size_t)i * e.max_seq], cs1 = cs[(size_t)(i + 1) * e.max_seq];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const float a = x[i + u] * (r * (u ? bf_hi(ga) : bf_lo(ga)));
                 const float b = y[i + u] * (r * (u ? bf_hi(gb) : bf_lo(gb)));
-                const float cn = u ? c2.z : c2.x, sn = u ? c2.w : c2.y;
+                const float cn = u ? cs1.x : cs0.x, sn = u ? cs1.y : cs0.y;
                 x[i + u] = a * cn - b * sn;
                 y[i + u] = b * cn + a * sn;
             }
@@ -502,11 +518,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tc_kernel(const __grid_c
         if (lane == 0) {   // ---- TMA producer: one stage ring across all of this CTA's units
             // B: BN rows in boxes of B_BOX rows stacked in shared memory (SwiGLU: the gate
             // rows, then the matching up rows)
+            const uint64_t wpol = policy_evict_first();
             auto load_b = [&](uint32_t s, int n0, int kb) {
 #pragma unroll
                 for (int b = 0; b < B_LOADS; ++b)
-                    tma_2d(sB + s * B_BYTES + b * B_BOX * 128, &tmB, kb * BK,
-                           GLU ? (b ? up_off + n0 : n0) : n0 + b * B_BOX, &full[s]);
+                    tma_2d_hint(sB + s * B_BYTES + b * B_BOX * 128, &tmB, kb * BK,
+                                GLU ? (b ? up_off + n0 : n0) : n0 + b * B_BOX, &full[s], wpol);
             };
             // The weights do not depend on the preceding kernel: the B tiles of the first
             // stages are requested before waiting for it, their A tiles after.
