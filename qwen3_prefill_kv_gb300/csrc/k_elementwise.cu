@@ -143,9 +143,39 @@ __global__ void __launch_bounds__(128) rmsnorm1024_bf16_kernel(const float* __re
                             pack_bf2(b.z * r * bf_lo(gb.y), b.w * r * bf_hi(gb.y)));
 }
 
+// H = 1024, many rows (a long prompt): one warp per row, 8 rows per block, each lane holding
+// 32 values (eight 16-byte loads in flight); the row's sum of squares is a warp reduction,
+// with no block barrier.
+__global__ void __launch_bounds__(256) rmsnorm1024_rows_kernel(const float* __restrict__ X, int T,
+                                                               const bf16_t* __restrict__ g, float eps,
+                                                               bf16_t* __restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (row >= T) return;
+    const float4* x = reinterpret_cast<const float4*>(X + (size_t)row * 1024);
+    float4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = x[lane + 32 * k];
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+    const float r = rsqrtf(warp_sum(ss) / 1024.f + eps);
+    const uint2* g2 = reinterpret_cast<const uint2*>(g);
+    uint2* o = reinterpret_cast<uint2*>(out + (size_t)row * 1024);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint2 gw = g2[lane + 32 * k];
+        o[lane + 32 * k] = make_uint2(pack_bf2(v[k].x * r * bf_lo(gw.x), v[k].y * r * bf_hi(gw.x)),
+                                      pack_bf2(v[k].z * r * bf_lo(gw.y), v[k].w * r * bf_hi(gw.y)));
+    }
+}
+
 cudaError_t launch_rmsnorm_bf16(const float* X, int T, int H, const bf16_t* g, float eps, bf16_t* out,
                                 cudaStream_t s) {
     (void)cudaGetLastError();   // attribute only this launch's errors
+    if (H == 1024 && T >= 1024)
+        return launch_pdl(rmsnorm1024_rows_kernel, dim3((T + 7) / 8), dim3(256), 0, s, X, T, g, eps, out);
     if (H == 1024) return launch_pdl(rmsnorm1024_bf16_kernel, dim3(T), dim3(128), 0, s, X, g, eps, out);
     return launch_pdl(rmsnorm_bf16_kernel, dim3(T), dim3(256), 0, s, X, H, g, eps, out);
 }
