@@ -96,6 +96,11 @@ __device__ __forceinline__ void tma_2d_hint(void* dst, const CUtensorMap* map, i
         "l"(map), "r"(x), "r"(y), "r"(s32(bar)), "l"(pol)
         : "memory");
 }
+// L2 prefetch of one box of a tensor map (no shared memory, no completion to wait for)
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(s32(slot)), "r"(ncols)
                  : "memory");
@@ -525,8 +530,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) gemm_tc_kernel(const __grid_c
                     tma_2d_hint(sB + s * B_BYTES + b * B_BOX * 128, &tmB, kb * BK,
                                 GLU ? (b ? up_off + n0 : n0) : n0 + b * B_BOX, &full[s], wpol);
             };
-            // The weights do not depend on the preceding kernel: the B tiles of the first
-            // stages are requested before waiting for it, their A tiles after.
+            // The weights do not depend on the preceding kernel: the whole weight matrix is
+            // prefetched into L2 (boxes dealt over the CTAs; a prefill streams each layer's
+            // weights from HBM once, and without it the first touch of a tile waits for HBM), and
+            // the B tiles of the first stages are requested, before waiting for it; their A tiles
+            // after.
+            {
+                const int wrows = GLU ? up_off + tiles_n * (BN / 2) : tiles_n * BN;
+                const int nb = ((wrows + B_BOX - 1) / B_BOX) * nkb;
+                for (int b = blockIdx.x; b < nb; b += gridDim.x) tma_prefetch_2d(&tmB, (b % nkb) * BK, (b / nkb) * B_BOX);
+            }
             uint32_t npre = 0;
             for (int u = blockIdx.x; u < units && npre < (uint32_t)STAGES; u += gridDim.x) {
                 int m0, nt, kb0, nk, z;
@@ -990,9 +1003,13 @@ cudaError_t launch_gemm_tc(const bf16_t* A, int lda, const bf16_t* W, int M, int
         case GEMM_ADD_F32: return launch_bn<128, GEMM_ADD_F32, 6>(ma, mb, mc, M, N, K, up_off, Cf, Cb, ldc, splits, s, QkvRopeEpi{}, bias, relu);
         case GEMM_SWIGLU_BF16: return launch_bn<128, GEMM_SWIGLU_BF16, 6>(ma, mb, mc, M, N, K, up_off, Cf, Cb, ldc, splits, s);
         case GEMM_STORE_BF16: return launch_bn<128, GEMM_STORE_BF16, 6>(ma, mb, mc, M, N, K, up_off, Cf, Cb, ldc, splits, s, QkvRopeEpi{}, bias, relu);
-        // split-K CTAs run few k-blocks each: a 3-stage ring (97 KB) lets two share an SM
+        // The lockstep batch's split-K CTAs run few k-blocks each: a 3-stage ring (97 KB) lets
+        // two share an SM.  The prefill's split-K launches have about one unit per SM and are
+        // launched while the preceding kernel still holds SMs: with two CTAs allowed per SM the
+        // first SMs to free up took two each (the 64-position prefill measured 1.55 against 1.33
+        // ms), so their 6-stage ring (193 KB) keeps one CTA per SM.
         case GEMM_ATOMIC_F32: return launch_bn<128, GEMM_ATOMIC_F32, 3>(ma, mb, mc, M, N, K, up_off, Cf, Cb, ldc, splits, s);
-        case GEMM_PARTIAL_F32: return launch_bn<128, GEMM_PARTIAL_F32, 3>(ma, mb, mc, M, N, K, up_off, Cf, Cb, ldc, splits, s);
+        case GEMM_PARTIAL_F32: return launch_bn<128, GEMM_PARTIAL_F32, 6>(ma, mb, mc, M, N, K, up_off, Cf, Cb, ldc, splits, s);
         default: return cudaErrorInvalidValue;
     }
 }
