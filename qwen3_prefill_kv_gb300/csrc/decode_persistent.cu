@@ -140,6 +140,20 @@ __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t
                  "l"(src), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
 }
+// The same with an L2 eviction-priority policy (createpolicy)
+__device__ __forceinline__ void tma_load_1d_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                                 uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+// L2 prefetch of `bytes` (a multiple of 16) at src (16-byte aligned) with a policy
+__device__ __forceinline__ void l2_prefetch_hint(const void* src, uint32_t bytes, uint64_t pol) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src), "r"(bytes), "l"(pol)
+                 : "memory");
+}
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory"); }
 
 __device__ __forceinline__ void ll_store(unsigned long long* p, uint32_t tag, float v) {
@@ -701,11 +715,28 @@ __global__ void __launch_bounds__(NT, 1) decode_persistent_kernel(const DecodePa
             uint32_t parity = 0;
             bool ok = true;
             const int n_ph = p.NL * PH_PER_LAYER + 1;
+            // The step streams every weight once (1.2 GB against a 129 MB L2): weight stages
+            // carry an evict-first policy, so they do not push out the KV history and the
+            // lm_head rows prefetched below.  The lm_head phase streams its 311 MB at the HBM
+            // roofline after the last layer, while the layers before it, bound by their
+            // hand-offs, use a fraction of HBM: during each of the last LM_PF_LAYERS layers
+            // this CTA prefetches another 1/LM_PF_DEN of its lm_head rows into L2 (evict-last).
+            constexpr int LM_PF_LAYERS = 3, LM_PF_DEN = 12;
+            uint64_t pol_w, pol_keep;
+            asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
+            asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_keep));
 #pragma unroll 1
             for (int t = 0; t < n_ph && ok; ++t) {
                 const int l = min(t / PH_PER_LAYER, p.NL - 1);
                 const int e = (t == n_ph - 1) ? PH_PER_LAYER : t - l * PH_PER_LAYER;
                 const DecodeLayer* Lw = p.layers + l;
+                if (e == 0 && l >= p.NL - LM_PF_LAYERS && l < p.NL) {
+                    const int nv = P.v1 - P.v0, k = l - (p.NL - LM_PF_LAYERS);
+                    const int a = P.v0 + (int)((long long)nv * k / LM_PF_DEN);
+                    const int b = P.v0 + (int)((long long)nv * (k + 1) / LM_PF_DEN);
+                    for (int r = a; r < b; r += 32)   // 32 rows (64 KB at H = 1024) a request
+                        l2_prefetch_hint(p.embed + (size_t)r * p.H, (uint32_t)(min(32, b - r) * p.H * 2), pol_keep);
+                }
                 const bf16_t *src0, *src1 = nullptr, *src_up = nullptr;
                 int i0, i1, per, stride, nsub = 1;
                 if (e == 0) {
@@ -734,8 +765,13 @@ __global__ void __launch_bounds__(NT, 1) decode_persistent_kernel(const DecodePa
                         }
                         mbar_expect_tx(&S.full[slot], src_up ? 2u * bytes : bytes);
                         char* dst = S.ring + (size_t)slot * SLOT;
-                        tma_load_1d(dst, (sub == 0 ? src0 : src1) + (size_t)i * stride, bytes, &S.full[slot]);
-                        if (src_up) tma_load_1d(dst + bytes, src_up + (size_t)i * stride, bytes, &S.full[slot]);
+                        if (e == 1) {   // the KV history: default policy
+                            tma_load_1d(dst, (sub == 0 ? src0 : src1) + (size_t)i * stride, bytes, &S.full[slot]);
+                        } else {
+                            tma_load_1d_hint(dst, src0 + (size_t)i * stride, bytes, &S.full[slot], pol_w);
+                            if (src_up)
+                                tma_load_1d_hint(dst + bytes, src_up + (size_t)i * stride, bytes, &S.full[slot], pol_w);
+                        }
                         ++issued;
                         if (++slot == S.nslot) {
                             slot = 0;
