@@ -1004,10 +1004,11 @@ cudaError_t launch_gemm_tc(const bf16_t* A, int lda, const bf16_t* W, int M, int
         case GEMM_SWIGLU_BF16: return launch_bn<128, GEMM_SWIGLU_BF16, 6>(ma, mb, mc, M, N, K, up_off, Cf, Cb, ldc, splits, s);
         case GEMM_STORE_BF16: return launch_bn<128, GEMM_STORE_BF16, 6>(ma, mb, mc, M, N, K, up_off, Cf, Cb, ldc, splits, s, QkvRopeEpi{}, bias, relu);
         // The lockstep batch's split-K CTAs run few k-blocks each: a 3-stage ring (97 KB) lets
-        // two share an SM.  The prefill's split-K launches have about one unit per SM and are
-        // launched while the preceding kernel still holds SMs: with two CTAs allowed per SM the
-        // first SMs to free up took two each (the 64-position prefill measured 1.55 against 1.33
-        // ms), so their 6-stage ring (193 KB) keeps one CTA per SM.
+        // two share an SM.  The prefill's split-K launches have about one unit per SM and start
+        // while the preceding kernel still holds SMs; in a build whose register count let two
+        // of their CTAs share an SM, the 64-position prefill took 1.55 against 1.33 ms (CTAs
+        // doubling up on the first SMs to free), so their 6-stage ring (193 KB) keeps one CTA
+        // per SM.
         case GEMM_ATOMIC_F32: return launch_bn<128, GEMM_ATOMIC_F32, 3>(ma, mb, mc, M, N, K, up_off, Cf, Cb, ldc, splits, s);
         case GEMM_PARTIAL_F32: return launch_bn<128, GEMM_PARTIAL_F32, 6>(ma, mb, mc, M, N, K, up_off, Cf, Cb, ldc, splits, s);
         default: return cudaErrorInvalidValue;
