@@ -55,3 +55,20 @@ def test_single_process_is_the_identity():
     import bench
     assert bench.reduce_max_over_ranks([3, 1.5], 1, "cpu") == [3.0, 1.5]
     assert bench.whole_job_rate(1, 100, 4.0) == 25.0
+
+
+def test_profiled_traffic_only_while_the_kernel_sources_match(tmp_path, monkeypatch):
+    """The decode roofline's DRAM traffic comes from an ncu capture: bench.py reports it only
+    while the decode kernel's source files hash to the value recorded with that capture, and
+    null once they change (or for a workload never captured)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    src = tmp_path / "kernel.cu"
+    src.write_text("// kernel source at the capture\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "DECODE_KERNEL_SOURCES", ("kernel.cu",))
+    monkeypatch.setattr(bench, "PROFILED_DECODE_TRAFFIC", {"w": (bench.decode_sources_sha(), 1234)})
+    assert bench.profiled_decode_traffic("w") == 1234
+    assert bench.profiled_decode_traffic("other") is None
+    src.write_text("// kernel source changed since the capture\n")
+    assert bench.profiled_decode_traffic("w") is None
