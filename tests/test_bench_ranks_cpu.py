@@ -1,7 +1,8 @@
-"""bench.py's multi-replica bookkeeping on CPU: with two gloo ranks, every rank gets the
+"""bench.py's bookkeeping on CPU.  Multi-replica: with two gloo ranks, every rank gets the
 element-wise maximum of the ranks' times (the slowest replica defines the job) and the
-whole-job rate counts every rank's units over that time.  The replicas share nothing
-else: the decoder path itself has no collective."""
+whole-job rate counts every rank's units over that time; the replicas share nothing else
+(the decoder path itself has no collective).  Roofline: the profiled DRAM traffic is
+reported only for the kernel sources it was captured with."""
 import os
 import socket
 import sys
